@@ -1,0 +1,591 @@
+"""Pins for the CPU oracle: it is checked against things other than itself.
+
+Each pin is a different route to the same answer -- brute force on tiny
+inputs built another way, a library routine the definition reduces to, a
+closed form the pages print, or an invariant the method fixes -- so that a
+plausible slip in the oracle (a dropped alignment, a wrong owner rank, an
+off-by-one in a prefix sum, a transposed scale layout, a wrong rounding mode)
+fails at least one of them.  ``test_planted_mistakes_are_caught`` plants such
+slips in copies of the oracle and checks that the pins notice.
+"""
+import itertools
+import os
+from collections import Counter
+
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from oracle import ep_oracle as O
+
+GOLDEN = os.path.join(os.path.dirname(__file__), "golden")
+
+
+# ---------------------------------------------------------------------------
+# Layout: brute force built from explicit lists
+# ---------------------------------------------------------------------------
+def brute_layout(idx, E, R, M, A, do_expand):
+    """Build the layout by appending rows to a Python list (no prefix sums)."""
+    T, K = len(idx), len(idx[0]) if len(idx) else 0
+    L = E // R
+    cnt_e = Counter(e for row in idx for e in row if e >= 0)
+    ranks_of_tok = [sorted({e // L for e in row if e >= 0}) for row in idx]
+    rows = []            # each entry: (t, k) or None for padding
+    dst = [[-1] * K for _ in range(T)]
+    if do_expand:
+        for e in range(E):
+            for t in range(T):
+                for k in range(K):
+                    if idx[t][k] == e:
+                        dst[t][k] = len(rows)
+                        rows.append((t, k))
+            while len(rows) % A:
+                rows.append(None)
+    else:
+        for r in range(R):
+            for t in range(T):
+                if r in ranks_of_tok[t]:
+                    ks = [k for k in range(K) if idx[t][k] >= 0 and idx[t][k] // L == r]
+                    for k in ks:
+                        dst[t][k] = len(rows)
+                    rows.append((t, ks[0]))
+    in_rank = [[r in ranks_of_tok[t] for r in range(R)] for t in range(T)]
+    cnt_rank = [sum(in_rank[t][r] for t in range(T)) for r in range(R)]
+    src_cnt = [[sum(1 for t in range(T) if t // M == s and in_rank[t][r]) for s in range(R)]
+               for r in range(R)]
+    return {"cnt_e": [cnt_e.get(e, 0) for e in range(E)], "rows": rows, "dst": dst,
+            "in_rank": in_rank, "cnt_rank": cnt_rank, "src_cnt": src_cnt}
+
+
+def check_layout_against_brute(layout_fn, idx, E, R, M, A, do_expand):
+    lay = layout_fn(np.array(idx, dtype=np.int64).reshape(len(idx), -1), E, R, M, A,
+                    do_expand, True)
+    b = brute_layout(idx, E, R, M, A, do_expand)
+    assert lay["cnt_expert"].tolist() == b["cnt_e"]
+    assert lay["dst_buffer_slot_idx"].tolist() == b["dst"]
+    assert lay["is_token_in_rank"].tolist() == b["in_rank"]
+    assert lay["cnt_rank"].tolist() == b["cnt_rank"]
+    assert lay["psum_rank"].tolist() == [sum(b["cnt_rank"][:r]) for r in range(R + 1)]
+    for r in range(R):
+        assert lay["psum_rank_src"][r].tolist() == [sum(b["src_cnt"][r][:s])
+                                                     for s in range(R + 1)]
+    assert lay["total_rows"] == len(b["rows"])
+    meta = lay["recv_src_metadata"][: len(b["rows"])].tolist()
+    assert meta == [list(x) if x is not None else [-1, -1] for x in b["rows"]]
+    if do_expand:
+        # segment starts: position of the first row of each expert in the list
+        starts, pos = [], 0
+        for e in range(E):
+            starts.append(pos)
+            pos += -(-b["cnt_e"][e] // A) * A
+        starts.append(pos)
+        assert lay["psum_expert"].tolist() == starts
+
+
+def _tiny_cases():
+    # all topk_idx over {-1..E-1} for small T, K, E, and every parameter mix
+    for T, K, E in [(1, 1, 2), (1, 2, 4), (2, 2, 2), (2, 1, 4), (2, 2, 4), (3, 2, 2)]:
+        for R in (1, 2):
+            if E % R:
+                continue
+            for vals in itertools.product(range(-1, E), repeat=T * K):
+                yield T, K, E, R, [list(vals[t * K:(t + 1) * K]) for t in range(T)]
+
+
+def test_layout_bruteforce_exhaustive_tiny():
+    n = 0
+    for T, K, E, R, idx in _tiny_cases():
+        for M in sorted({-(-T // R), T}):
+            for A in (1, 3):
+                for do_expand in (False, True):
+                    check_layout_against_brute(O.layout, idx, E, R, M, A, do_expand)
+                    n += 1
+    assert n > 5000
+
+
+@pytest.mark.parametrize("seed", [0, 1, 2])
+def test_layout_bruteforce_random_medium(seed):
+    rng = np.random.default_rng(seed)
+    for _ in range(6):
+        T, K = int(rng.integers(1, 40)), int(rng.integers(1, 5))
+        R = int(rng.choice([1, 2, 4]))
+        E = R * int(rng.integers(1, 5))
+        M = int(rng.integers(-(-T // R), T + 1))
+        A = int(rng.choice([1, 2, 4, 8]))
+        idx = rng.integers(-1, E, size=(T, K)).tolist()
+        for do_expand in (False, True):
+            check_layout_against_brute(O.layout, idx, E, R, M, A, do_expand)
+
+
+def test_layout_one_rank_is_stable_counting_sort():
+    """R = 1, A = 1: the expanded rows are a stable sort of the slots by expert."""
+    rng = np.random.default_rng(7)
+    idx = rng.integers(-1, 12, size=(300, 5))
+    lay = O.layout(idx, 12, 1, 300, 1, True, True)
+    flat = idx.reshape(-1)
+    valid = np.flatnonzero(flat >= 0)
+    order = valid[np.argsort(flat[valid], kind="stable")]
+    expect = np.full(flat.size, -1)
+    expect[order] = np.arange(order.size)
+    assert np.array_equal(lay["dst_buffer_slot_idx"].reshape(-1), expect)
+    assert np.array_equal(lay["cnt_expert"], np.bincount(flat[valid], minlength=12))
+
+
+def check_layout_invariants(lay, topk_idx):
+    T, K, E, R, L, A = lay["T"], lay["K"], lay["E"], lay["R"], lay["L"], lay["A"]
+    idx = np.asarray(topk_idx)
+    valid = (idx >= 0) & (idx < E)
+    assert lay["cnt_expert"].sum() == valid.sum()
+    assert np.all(lay["cnt_expert_aligned"] % A == 0)
+    assert np.all(lay["cnt_expert_aligned"] - lay["cnt_expert"] < A)
+    assert np.all(np.diff(lay["psum_expert"]) >= 0) and lay["psum_expert"][0] == 0
+    assert lay["cnt_rank"].sum() == lay["is_token_in_rank"].sum()
+    assert np.array_equal(lay["psum_rank_src"][:, R], lay["cnt_rank"])
+    for r in range(R):
+        # a token is on rank r iff one of its experts is in r's block of L
+        on = ((idx // L == r) & valid).any(axis=1)
+        assert np.array_equal(lay["is_token_in_rank"][:, r], on)
+    dst, meta = lay["dst_buffer_slot_idx"], lay["recv_src_metadata"]
+    if lay["do_expand"]:
+        v = dst[valid]
+        assert np.unique(v).size == v.size                 # injective
+        tt, kk = np.nonzero(valid)
+        assert np.array_equal(meta[dst[tt, kk]], np.stack([tt, kk], 1))
+        for e in range(E):
+            s0, c = lay["psum_expert"][e], lay["cnt_expert"][e]
+            assert s0 % A == 0
+            seg = meta[s0:s0 + c, 0]
+            assert np.all(np.diff(seg) >= 0)                # ascending source token
+            assert np.all(idx[meta[s0:s0 + c, 0], meta[s0:s0 + c, 1]] == e)
+            assert np.all(meta[s0 + c:lay["psum_expert"][e + 1]] == -1)
+    else:
+        tt, kk = np.nonzero(valid)
+        rows = dst[tt, kk]
+        assert np.all(meta[rows, 0] == tt)
+        assert np.all(idx[tt, meta[rows, 1]] // L == idx[tt, kk] // L)
+        for r in range(R):
+            seg = meta[lay["psum_rank"][r]:lay["psum_rank"][r + 1], 0]
+            assert np.all(np.diff(seg) > 0)                 # one row per token, ascending
+
+
+@pytest.mark.parametrize("name", ["tiny", "decode", "prefill", "skewed"])
+def test_layout_invariants_workloads(name):
+    import ep_workloads as W
+    wl = W.WORKLOADS[name]
+    T = min(wl.num_tokens, 2048)
+    idx, _ = W.make_routing(wl, seed=3, num_tokens=T)
+    lay = O.layout(idx.numpy(), wl.num_experts, wl.num_ranks, max(wl.num_max_tokens_per_rank,
+                   -(-T // wl.num_ranks)), wl.expert_alignment, wl.do_expand, True)
+    check_layout_invariants(lay, idx.numpy())
+    for de in (not wl.do_expand,):
+        lay2 = O.layout(idx.numpy(), wl.num_experts, wl.num_ranks,
+                        max(wl.num_max_tokens_per_rank, -(-T // wl.num_ranks)),
+                        wl.expert_alignment, de, True)
+        check_layout_invariants(lay2, idx.numpy())
+
+
+def test_layout_bad_index_is_flagged_and_dropped():
+    idx = np.array([[0, 5], [-2, 1], [3, -1]])
+    lay = O.layout(idx, 4, 2, 2, 1, True, True)
+    assert lay["error"] & 1
+    assert lay["dst_buffer_slot_idx"][0, 1] == -1 and lay["dst_buffer_slot_idx"][1, 0] == -1
+    assert lay["cnt_expert"].tolist() == [1, 1, 0, 1]
+
+
+# ---------------------------------------------------------------------------
+# Upper-bound allocation: the expressions printed in the pages (§7.2)
+# ---------------------------------------------------------------------------
+def _golden_bounds():
+    out = []
+    with open(os.path.join(GOLDEN, "upper_bound_rows.txt")) as f:
+        for line in f:
+            line = line.strip()
+            if not line or line.startswith("#"):
+                continue
+            name, *nums = line.split()
+            out.append((name, *map(int, nums)))
+    return out
+
+
+@pytest.mark.parametrize("row", _golden_bounds(), ids=lambda r: r[0])
+def test_upper_bound_golden(row):
+    name, T, K, E, R, M, A, de, per_rank, glob, rows = row
+    assert O.upper_bound_rows(T, K, E, R, M, A, bool(de), parts=True) == (per_rank, glob, rows)
+
+
+def test_upper_bound_holds_and_overflow_is_flagged():
+    rng = np.random.default_rng(11)
+    for _ in range(200):
+        R = int(rng.choice([1, 2, 4]))
+        E = R * int(rng.integers(1, 5))
+        K = int(rng.integers(1, E + 1))
+        M = int(rng.integers(1, 6))
+        T = int(rng.integers(0, M * R + 1))
+        A = int(rng.choice([1, 2, 4]))
+        # distinct experts per token (the per-rank bound's assumption)
+        idx = np.array([rng.permutation(E)[:K] for _ in range(T)]).reshape(T, K)
+        idx[rng.random((T, K)) < 0.1] = -1
+        for de in (False, True):
+            lay = O.layout(idx, E, R, M, A, de, False)
+            assert lay["total_rows"] <= lay["rows_alloc"]
+            assert lay["error"] == 0
+            per_rank = O.upper_bound_rows(T, K, E, R, M, A, de, parts=True)[0]
+            starts = lay["psum_expert"][::E // R] if de else lay["psum_rank"]
+            assert np.all(np.diff(starts) <= per_rank)
+    # repeated experts can exceed the printed bound: rows past it are dropped
+    idx = np.array([[0, 0, 0, 0], [1, 1, 0, 0]])
+    lay = O.layout(idx, 2, 2, 1, 1, True, False)
+    assert lay["rows_alloc"] == 4 and lay["total_rows"] == 8
+    assert lay["error"] & 2
+    assert np.all(lay["dst_buffer_slot_idx"] < 4)
+    assert (lay["dst_buffer_slot_idx"] >= 0).sum() == 4
+
+
+# ---------------------------------------------------------------------------
+# Number formats: library special cases
+# ---------------------------------------------------------------------------
+def _e4m3_grid():
+    codes = np.array([c for c in range(256) if c & 0x7F != 0x7F], dtype=np.uint8)
+    vals = np.sort(np.unique(O.e4m3_decode(codes)))
+    mids = (vals[:-1] + vals[1:]) / 2                      # exact ties
+    f32 = np.float32
+    pts = [vals, mids, np.nextafter(mids.astype(f32), f32(np.inf)),
+           np.nextafter(mids.astype(f32), f32(-np.inf))]
+    rng = np.random.default_rng(5)
+    pts += [rng.uniform(-448, 448, 20000), rng.normal(0, 1, 20000),
+            rng.normal(0, 2 ** -7, 20000), np.ldexp(rng.uniform(-1, 1, 5000), -12),
+            rng.uniform(448, 463.99, 100), -rng.uniform(448, 463.99, 100)]
+    return np.concatenate(pts).astype(np.float32)
+
+
+def test_e4m3_encode_matches_torch_in_range():
+    v = _e4m3_grid()
+    got = O.e4m3_encode(v)
+    ref = torch.from_numpy(v).to(torch.float8_e4m3fn).view(torch.uint8).numpy()
+    assert np.array_equal(got, ref)
+
+
+def test_e4m3_saturation_and_specials():
+    v = np.array([464.0, 479.0, 480.0, 1e4, np.inf, -np.inf, -1e9, np.nan, -0.0, 0.0,
+                  2.0 ** -10, 3 * 2.0 ** -10, 2.0 ** -20], dtype=np.float32)
+    got = O.e4m3_encode(v).tolist()
+    assert got == [0x7E, 0x7E, 0x7E, 0x7E, 0x7E, 0xFE, 0xFE, 0x7F, 0x80, 0x00,
+                   0x00, 0x02, 0x00]
+    # every finite code decodes and re-encodes to itself
+    codes = np.array([c for c in range(256) if c & 0x7F != 0x7F], dtype=np.uint8)
+    assert np.array_equal(O.e4m3_encode(O.e4m3_decode(codes).astype(np.float32)), codes)
+
+
+def test_bf16_round_trip_matches_torch():
+    rng = np.random.default_rng(2)
+    f = np.concatenate([rng.normal(0, 1, 50000), rng.normal(0, 1e30, 1000),
+                        rng.normal(0, 1e-38, 1000),
+                        [0.0, -0.0, np.inf, -np.inf, 3.3895314e38, -3.3895314e38,
+                         1.0 + 2 ** -8, 1.0 + 3 * 2 ** -8, 1.0 + 2 ** -8 + 2 ** -20]]
+                       ).astype(np.float32)
+    got = O.f32_to_bf16_bits(f)
+    ref = torch.from_numpy(f).to(torch.bfloat16).view(torch.int16).numpy().view(np.uint16)
+    assert np.array_equal(got, ref)
+    assert np.isnan(O.bf16_bits_to_f32(O.f32_to_bf16_bits(np.array([np.nan], np.float32))))[0]
+    back = O.bf16_bits_to_f32(ref)
+    assert np.array_equal(back, torch.from_numpy(ref.view(np.int16)).view(torch.bfloat16)
+                          .float().numpy())
+
+
+# ---------------------------------------------------------------------------
+# FP8 quantisation: library special case + error bounds + closed forms
+# ---------------------------------------------------------------------------
+def _bf16(a):
+    return torch.from_numpy(np.asarray(a, np.float32)).to(torch.bfloat16).view(
+        torch.int16).numpy().view(np.uint16)
+
+
+def check_quantize(quant_fn, x_bits):
+    q, s = quant_fn(x_bits)
+    x = O.bf16_bits_to_f32(x_bits).reshape(x_bits.shape[0], -1, 128)
+    amax = np.abs(x).max(axis=2)
+    # scale: one fp32 IEEE division (torch's fp32 division is the library check)
+    s_ref = (torch.from_numpy(amax) / torch.tensor(448.0, dtype=torch.float32)).numpy()
+    assert np.array_equal(s, s_ref)
+    qb = q.reshape(x.shape)
+    nz = s > 0
+    ratio = torch.from_numpy(x) / torch.from_numpy(np.where(nz, s, 1))[..., None]
+    ref = ratio.to(torch.float8_e4m3fn).view(torch.uint8).numpy()
+    ref = np.where(nz[..., None], ref, 0)
+    assert np.array_equal(qb, ref)
+    # dequantised error bounds (normal: half an ulp is 2^-4 relative; subnormal 2^-10)
+    deq = O.e4m3_decode(qb) * s[..., None]
+    err = np.abs(deq - x)
+    tiny = np.abs(x) < (2.0 ** -6) * s[..., None]
+    assert np.all(err[~tiny] <= 2.0 ** -4 * np.abs(x[~tiny]) + 1e-30)
+    assert np.all(err[tiny] <= 2.0 ** -10 * np.broadcast_to(s[..., None], x.shape)[tiny] * 1.0001)
+    # the element holding amax lands on 448 (0x7E) or one step below it
+    am = np.abs(x).argmax(axis=2)
+    top = np.take_along_axis(qb, am[..., None], 2)[..., 0] & 0x7F
+    assert np.all((top[nz] == 0x7E) | (top[nz] == 0x7D))
+    assert np.all(qb[~nz] == 0)
+
+
+def test_quantize_row_pins():
+    rng = np.random.default_rng(9)
+    x = rng.normal(0, 1, (64, 512)).astype(np.float32)
+    x[3, :128] = 0.0                       # all-zero block -> scale 0, bytes 0
+    x[4, 128:256] = -0.0
+    x[5, 256:384] *= 1e-36                 # subnormal-range scale
+    x[6] = rng.standard_cauchy(512)        # wide dynamic range in a block
+    x[7, :128] = 1.0                       # constant block
+    check_quantize(O.quantize_row, _bf16(x))
+
+
+# ---------------------------------------------------------------------------
+# Dispatch: identity of the copy, per-row metadata, padding
+# ---------------------------------------------------------------------------
+def test_dispatch_bf16_copy_identity_and_padding():
+    rng = np.random.default_rng(4)
+    T, K, E, R, H = 50, 3, 8, 4, 64
+    idx = np.array([rng.permutation(E)[:K] for _ in range(T)])
+    idx[rng.random((T, K)) < 0.2] = -1
+    w = rng.random((T, K)).astype(np.float32)
+    xb = _bf16(rng.normal(0, 1, (T, H)))
+    for de in (True, False):
+        lay = O.layout(idx, E, R, 13, 4, de, True)
+        d = O.dispatch(lay, xb, w, use_fp8=False, do_zero_padding=True)
+        tt, kk = np.nonzero(idx >= 0)
+        rows = lay["dst_buffer_slot_idx"][tt, kk]
+        assert np.array_equal(d["recv_x"][rows], xb[tt])
+        if de:
+            assert np.array_equal(d["recv_topk_weights"][rows], w[tt, kk])
+            assert np.all(d["recv_x"][d["padding"]] == 0)
+            assert np.all(d["recv_topk_weights"][d["padding"]] == 0)
+        else:
+            L = E // R
+            assert np.array_equal(d["recv_topk_weights"][rows, kk], w[tt, kk])
+            assert np.array_equal(d["recv_topk_idx"][rows, kk], idx[tt, kk] - (idx[tt, kk] // L) * L)
+            # entries of other ranks' slots are 0 / -1
+            n_on = (d["recv_topk_idx"][:lay["total_rows"]] >= 0).sum()
+            assert n_on == (idx >= 0).sum()
+
+
+def test_dispatch_fp8_scale_layouts():
+    rng = np.random.default_rng(8)
+    T, K, E, R, H = 20, 2, 4, 2, 256
+    idx = np.array([rng.permutation(E)[:K] for _ in range(T)])
+    xb = _bf16(rng.normal(0, 1, (T, H)))
+    lay = O.layout(idx, E, R, 10, 8, True, True)
+    q, s = O.quantize_row(xb)
+    rows_alloc = lay["rows_alloc"]
+    for cm in (True, False):
+        d = O.dispatch(lay, xb, None, use_fp8=True, col_major_sf=cm, do_zero_padding=True)
+        sf = d["recv_sf"]
+        stride = -(-rows_alloc // 4) * 4
+        assert sf.size == (H // 128) * (stride if cm else rows_alloc)
+        sf2 = sf.reshape(H // 128, stride).T if cm else sf.reshape(rows_alloc, H // 128)
+        tt, kk = np.nonzero(idx >= 0)
+        rows = lay["dst_buffer_slot_idx"][tt, kk]
+        assert np.array_equal(sf2[rows], s[tt])
+        assert np.array_equal(d["recv_x"][rows], q[tt])
+        assert np.all(sf2[:rows_alloc][d["padding"]] == 0)
+
+
+# ---------------------------------------------------------------------------
+# Combine: fp64 brute force, identity experts, special cases
+# ---------------------------------------------------------------------------
+def _ulp_diff(a_bits, b_bits):
+    a = a_bits.astype(np.int32)
+    b = b_bits.astype(np.int32)
+    # map sign-magnitude to a monotone integer line
+    a = np.where(a & 0x8000, -(a & 0x7FFF), a)
+    b = np.where(b & 0x8000, -(b & 0x7FFF), b)
+    return np.abs(a - b)
+
+
+def check_combine_fp64(combine_fn, seed):
+    rng = np.random.default_rng(seed)
+    T, K, E, R, H = 40, 4, 8, 2, 96
+    idx = rng.integers(-1, E, (T, K))
+    w = rng.random((T, K)).astype(np.float32)
+    for de in (True, False):
+        lay = O.layout(idx, E, R, 20, 2, de, True)
+        rows = lay["rows_alloc"]
+        y = _bf16(rng.normal(0, 1, (rows, H)))
+        b0, b1 = _bf16(rng.normal(0, 1, (T, H))), _bf16(rng.normal(0, 1, (T, H)))
+        eb = _bf16(rng.normal(0, 0.1, (E, H)))
+        for weights in (w, None):
+            out = combine_fn(lay, y, weights, b0, b1, eb)
+            yf = O.bf16_bits_to_f32(y).astype(np.float64)
+            ebf = O.bf16_bits_to_f32(eb).astype(np.float64)
+            ref = O.bf16_bits_to_f32(b0).astype(np.float64) + O.bf16_bits_to_f32(b1)
+            dst = lay["dst_buffer_slot_idx"]
+            for t in range(T):
+                seen = set()
+                for k in range(K):
+                    r = dst[t, k]
+                    if r < 0 or (weights is None and r in seen):
+                        continue
+                    seen.add(r)
+                    wk = 1.0 if weights is None else float(weights[t, k])
+                    ref[t] += wk * (yf[r] + ebf[idx[t, k]])
+            ref_bits = _bf16(ref.astype(np.float32))
+            assert _ulp_diff(out, ref_bits).max() <= 1
+
+
+@pytest.mark.parametrize("seed", [0, 1])
+def test_combine_against_fp64(seed):
+    check_combine_fp64(O.combine, seed)
+
+
+def test_combine_identity_experts_return_x():
+    """y = dispatched x, weights summing to 1: combine gives x back."""
+    rng = np.random.default_rng(12)
+    T, K, E, R, H = 64, 4, 16, 4, 128
+    idx = np.array([rng.permutation(E)[:K] for _ in range(T)])
+    logits = rng.normal(0, 1, (T, K))
+    w = (np.exp(logits) / np.exp(logits).sum(1, keepdims=True)).astype(np.float32)
+    xb = _bf16(rng.normal(0, 1, (T, H)))
+    lay = O.layout(idx, E, R, 16, 8, True, True)
+    y = O.dispatch(lay, xb, w)["recv_x"]
+    out = O.combine(lay, y, w)
+    # |sum w - 1| is a few fp32 ulps, so the result is within one BF16 ulp of x
+    assert _ulp_diff(out, xb).max() <= 1
+    assert (out == xb).mean() > 0.95
+
+
+def test_combine_single_slot_and_empty_tokens():
+    rng = np.random.default_rng(13)
+    T, K, E, R, H = 6, 3, 4, 2, 32
+    idx = np.full((T, K), -1)
+    idx[0, 1] = 2
+    idx[1, 0] = 3
+    lay = O.layout(idx, E, R, 3, 1, True, True)
+    y = _bf16(rng.normal(0, 1, (lay["rows_alloc"], H)))
+    w = np.zeros((T, K), np.float32)
+    w[0, 1] = w[1, 0] = 1.0
+    out = O.combine(lay, y, w)
+    assert np.array_equal(out[0], y[lay["dst_buffer_slot_idx"][0, 1]])
+    assert np.array_equal(out[1], y[lay["dst_buffer_slot_idx"][1, 0]])
+    assert np.all(out[2:] == 0)
+    b0 = _bf16(rng.normal(0, 1, (T, H)))
+    b1 = _bf16(rng.normal(0, 1, (T, H)))
+    out = O.combine(lay, y, w, b0, b1)
+    s = O.bf16_bits_to_f32(b0) + O.bf16_bits_to_f32(b1)
+    assert np.array_equal(out[2:], _bf16(s[2:]))
+
+
+def test_combine_rank_layout_without_weights_counts_each_row_once():
+    idx = np.array([[0, 1, 2], [1, -1, 1]])   # E=4, R=2 -> L=2: slots 0,1 share rank 0
+    lay = O.layout(idx, 4, 2, 1, 1, False, True)
+    H = 16
+    y = _bf16(np.arange(lay["rows_alloc"] * H, dtype=np.float32).reshape(-1, H) / 8)
+    out = O.bf16_bits_to_f32(O.combine(lay, y, None))
+    d = lay["dst_buffer_slot_idx"]
+    yf = O.bf16_bits_to_f32(y)
+    assert d[0, 0] == d[0, 1] != d[0, 2]
+    assert np.array_equal(out[0], yf[d[0, 0]] + yf[d[0, 2]])
+    assert np.array_equal(out[1], yf[d[1, 0]])
+
+
+# ---------------------------------------------------------------------------
+# Planted mistakes: every one must be caught by some pin above
+# ---------------------------------------------------------------------------
+def _mutant_layout(kind):
+    def f(topk_idx, E, R, M, A=1, do_expand=False, do_cpu_sync=True):
+        if kind == "no_align":
+            return O.layout(topk_idx, E, R, M, 1, do_expand, do_cpu_sync)
+        if kind == "owner_mod":           # expert owner e % R instead of e // L
+            idx = np.asarray(topk_idx).copy()
+            L = E // R
+            m = idx >= 0
+            idx[m] = (idx[m] % R) * L + (idx[m] // R) % L
+            return O.layout(idx, E, R, M, A, do_expand, do_cpu_sync)
+        if kind == "inclusive_psum":
+            lay = O.layout(topk_idx, E, R, M, A, do_expand, do_cpu_sync)
+            lay["psum_rank"] = np.concatenate([np.cumsum(lay["cnt_rank"]), [lay["psum_rank"][-1]]])
+            return lay
+        if kind == "src_rank_off_by_one":
+            lay = O.layout(topk_idx, E, R, M, A, do_expand, do_cpu_sync)
+            p = lay["psum_rank_src"].copy()
+            p[:, 1:] = p[:, :-1]
+            lay["psum_rank_src"] = p
+            return lay
+        if kind == "descending_tokens":
+            idx = np.asarray(topk_idx)[::-1]
+            lay = O.layout(idx, E, R, M, A, do_expand, do_cpu_sync)
+            lay["dst_buffer_slot_idx"] = lay["dst_buffer_slot_idx"][::-1]
+            lay["is_token_in_rank"] = lay["is_token_in_rank"][::-1]
+            return lay
+        raise AssertionError(kind)
+    return f
+
+
+def _mutant_quant(kind):
+    def f(x_bits):
+        if kind == "mul_by_inverse":
+            x = O.bf16_bits_to_f32(x_bits).reshape(x_bits.shape[0], -1, 128)
+            amax = np.abs(x).max(axis=2)
+            s = (amax / np.float32(448)).astype(np.float32)
+            inv = (np.float32(448) / np.where(amax > 0, amax, 1)).astype(np.float32)
+            q = O.e4m3_encode((x * inv[..., None]).astype(np.float32))
+            return np.where(amax[..., None] > 0, q, 0).reshape(x_bits.shape).astype(np.uint8), s
+        if kind == "truncate":
+            q, s = O.quantize_row(x_bits)
+            x = O.bf16_bits_to_f32(x_bits).reshape(x_bits.shape[0], -1, 128)
+            r = (x / np.where(s > 0, s, 1)[..., None]).astype(np.float32)
+            t = torch.from_numpy(np.trunc(r * 8) / 8).to(torch.float8_e4m3fn).view(torch.uint8)
+            return np.where(s[..., None] > 0, t.numpy(), 0).reshape(x_bits.shape).astype(np.uint8), s
+        if kind == "scale_448_over":
+            q, s = O.quantize_row(x_bits)
+            return q, (s * np.float32(1.0000001)).astype(np.float32)
+        raise AssertionError(kind)
+    return f
+
+
+def _mutant_combine(kind):
+    def f(lay, y, w=None, b0=None, b1=None, eb=None):
+        if kind == "bias_before_weight_dropped":
+            return O.combine(lay, y, w, b0, b1, None)
+        if kind == "no_dedupe":
+            lay2 = dict(lay)
+            return O.combine(lay2, y, None if w is None else w, b0, b1, eb) if w is not None \
+                else _combine_no_dedupe(lay, y, b0, b1, eb)
+        if kind == "drop_bias1":
+            return O.combine(lay, y, w, b0, None, eb)
+        raise AssertionError(kind)
+    return f
+
+
+def _combine_no_dedupe(lay, y, b0, b1, eb):
+    T, K = lay["topk_idx"].shape
+    return O.combine(lay, y, np.ones((T, K), np.float32), b0, b1, eb)
+
+
+@pytest.mark.parametrize("kind", ["no_align", "owner_mod", "inclusive_psum",
+                                  "src_rank_off_by_one", "descending_tokens"])
+def test_planted_layout_mistakes_are_caught(kind):
+    bad = _mutant_layout(kind)
+    caught = False
+    rng = np.random.default_rng(21)
+    for _ in range(20):
+        T, K, R = 12, 3, 2
+        E, M, A = 8, 6, 4
+        idx = rng.integers(-1, E, (T, K)).tolist()
+        for de in (True, False):
+            try:
+                check_layout_against_brute(bad, idx, E, R, M, A, de)
+            except AssertionError:
+                caught = True
+    assert caught, kind
+
+
+@pytest.mark.parametrize("kind", ["mul_by_inverse", "truncate", "scale_448_over"])
+def test_planted_quant_mistakes_are_caught(kind):
+    rng = np.random.default_rng(22)
+    x = _bf16(rng.normal(0, 1, (64, 512)))
+    with pytest.raises(AssertionError):
+        check_quantize(_mutant_quant(kind), x)
+
+
+@pytest.mark.parametrize("kind", ["bias_before_weight_dropped", "no_dedupe", "drop_bias1"])
+def test_planted_combine_mistakes_are_caught(kind):
+    with pytest.raises(AssertionError):
+        check_combine_fp64(_mutant_combine(kind), 0)

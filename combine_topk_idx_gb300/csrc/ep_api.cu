@@ -1,0 +1,485 @@
+// Host side of libep.so: argument checks, sizing, handle ownership, launches.
+//
+// The contract (who allocates what, exact vs upper-bound sizes, handle
+// contents) follows "DeepEP V2 notes, ch. 7: how V2 dispatch builds expert
+// inputs" §7.1, §7.2 and §7.5, and "ch. 8: combine, handle and async
+// overlap" §8.1 / §8.2 (everything is ordered on the caller's stream).
+#include <chrono>
+#include <mutex>
+#include <thread>
+#include <vector>
+
+#include "ep_internal.cuh"
+
+struct ep_handle {
+  ep_config cfg;
+  int device;
+  cudaStream_t stream;
+  void *dmem;
+  ep::LayoutParams lp;
+  int64_t rows_alloc;
+  int64_t sf_hidden_stride, sf_token_stride, sf_numel;
+  float *tok_scale;
+};
+
+namespace ep {
+
+int device_sm_count(int device) {
+  static std::mutex mu;
+  static std::vector<int> cache;
+  std::lock_guard<std::mutex> g(mu);
+  if (device < 0) return 1;
+  if ((int)cache.size() <= device) cache.resize(device + 1, 0);
+  if (cache[device] == 0) {
+    int n = 0;
+    if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, device) != cudaSuccess || n < 1)
+      n = 1;
+    cache[device] = n;
+  }
+  return cache[device];
+}
+
+namespace {
+
+inline int64_t align_up(int64_t x, int64_t a) { return (x + a - 1) / a * a; }
+
+bool aligned(const void *p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
+
+struct Bounds {
+  int64_t per_rank, global, rows;
+};
+
+Bounds upper_bound(const ep_config &c) {
+  const int64_t T = c.num_tokens, K = c.num_topk, E = c.num_experts, R = c.num_ranks;
+  const int64_t L = E / R, M = c.num_max_tokens_per_rank, A = c.expert_alignment;
+  Bounds b;
+  if (c.do_expand) {
+    b.per_rank = align_up(R * M * std::min(K, L) + (A - 1) * L, A);
+    b.global = align_up(T * K + E * (A - 1), A);
+  } else {
+    b.per_rank = M * R;
+    b.global = T * std::min(K, R);
+  }
+  b.rows = std::min(R * b.per_rank, b.global);
+  return b;
+}
+
+// Pool of pinned, device-mapped host words for the count wait.
+struct SyncPool {
+  std::mutex mu;
+  std::vector<HostSync *> free_list;
+  int32_t seq = 0;
+  HostSync *acquire(int32_t *seq_out) {
+    std::lock_guard<std::mutex> g(mu);
+    *seq_out = ++seq;
+    if (seq > 0x3fffffff) seq = 0;
+    if (free_list.empty()) {
+      const int n = 64;
+      void *mem = nullptr;
+      if (cudaHostAlloc(&mem, n * sizeof(HostSync), cudaHostAllocMapped | cudaHostAllocPortable) !=
+          cudaSuccess)
+        return nullptr;
+      HostSync *s = static_cast<HostSync *>(mem);
+      for (int i = 0; i < n; ++i) free_list.push_back(s + i);
+    }
+    HostSync *h = free_list.back();
+    free_list.pop_back();
+    return h;
+  }
+  void release(HostSync *h) {
+    std::lock_guard<std::mutex> g(mu);
+    free_list.push_back(h);
+  }
+};
+
+SyncPool &sync_pool() {
+  static SyncPool *p = new SyncPool();  // never destroyed: kernels may still hold slots at exit
+  return *p;
+}
+
+// A memory pool per device for handle metadata: freed blocks are kept for
+// reuse (release threshold = max), so steady-state ep_layout calls do not map
+// new device memory.  Lives until process exit.
+cudaError_t handle_pool(int device, cudaMemPool_t *out) {
+  static std::mutex mu;
+  static std::vector<cudaMemPool_t> pools;
+  std::lock_guard<std::mutex> g(mu);
+  if ((int)pools.size() <= device) pools.resize(device + 1, nullptr);
+  if (pools[device] == nullptr) {
+    cudaMemPoolProps props{};
+    props.allocType = cudaMemAllocationTypePinned;
+    props.handleTypes = cudaMemHandleTypeNone;
+    props.location.type = cudaMemLocationTypeDevice;
+    props.location.id = device;
+    cudaMemPool_t pool = nullptr;
+    cudaError_t e = cudaMemPoolCreate(&pool, &props);
+    if (e != cudaSuccess) return e;
+    uint64_t threshold = ~0ull;
+    e = cudaMemPoolSetAttribute(pool, cudaMemPoolAttrReleaseThreshold, &threshold);
+    if (e != cudaSuccess) return e;
+    pools[device] = pool;
+  }
+  *out = pools[device];
+  return cudaSuccess;
+}
+
+ep_status cuda_status(cudaError_t e) {
+  if (e == cudaSuccess) return EP_OK;
+  if (e == cudaErrorMemoryAllocation) return EP_ERR_OOM;
+  return EP_ERR_CUDA;
+}
+
+}  // namespace
+}  // namespace ep
+
+using ep::align_up;
+using ep::aligned;
+
+extern "C" {
+
+const char *ep_status_string(ep_status s) {
+  switch (s) {
+    case EP_OK: return "ok";
+    case EP_ERR_INVALID_ARG: return "invalid argument";
+    case EP_ERR_UNSUPPORTED: return "unsupported configuration";
+    case EP_ERR_BAD_TOPK_IDX: return "topk_idx value outside [-1, num_experts)";
+    case EP_ERR_CUDA: return "CUDA runtime error";
+    case EP_ERR_OOM: return "out of memory";
+    case EP_ERR_TIMEOUT: return "timed out waiting for the receive counts";
+    case EP_ERR_OVERFLOW: return "upper-bound allocation exceeded";
+  }
+  return "unknown status";
+}
+
+int32_t ep_abi_version(void) { return EP_ABI_VERSION; }
+
+ep_status ep_validate_config(const ep_config *c) {
+  if (c == nullptr) return EP_ERR_INVALID_ARG;
+  if (c->num_tokens < 0 || c->num_topk < 1 || c->num_experts < 1 || c->num_ranks < 1 ||
+      c->hidden < 1 || c->num_max_tokens_per_rank < 1 || c->expert_alignment < 1 ||
+      c->num_sms < 0 || c->cpu_sync_timeout_ms < 0)
+    return EP_ERR_INVALID_ARG;
+  if (c->num_experts % c->num_ranks != 0) return EP_ERR_INVALID_ARG;
+  if (c->hidden % 8 != 0) return EP_ERR_INVALID_ARG;
+  if (c->use_fp8 && c->hidden % 128 != 0) return EP_ERR_INVALID_ARG;
+  if ((int64_t)c->num_tokens > (int64_t)c->num_max_tokens_per_rank * c->num_ranks)
+    return EP_ERR_INVALID_ARG;
+  if (c->topk_idx_is_int64 != 0 && c->topk_idx_is_int64 != 1) return EP_ERR_INVALID_ARG;
+  if (c->do_expand > 1 || c->do_zero_padding > 1 || c->do_cpu_sync > 1 || c->use_fp8 > 1 ||
+      c->use_tma_aligned_col_major_sf > 1)
+    return EP_ERR_INVALID_ARG;
+  if (c->reserved0[0] | c->reserved0[1] | c->reserved0[2]) return EP_ERR_INVALID_ARG;
+  if (c->num_topk > EP_MAX_TOPK || c->num_experts > EP_MAX_EXPERTS || c->hidden > EP_MAX_HIDDEN)
+    return EP_ERR_UNSUPPORTED;
+  const ep::Bounds b = ep::upper_bound(*c);
+  const int64_t lim = 0x7fffffffLL;
+  if ((int64_t)c->num_tokens * c->num_topk > lim || b.global > lim ||
+      (int64_t)c->num_tokens * c->num_ranks > (int64_t)1 << 40)
+    return EP_ERR_UNSUPPORTED;
+  return EP_OK;
+}
+
+ep_status ep_upper_bound_rows(const ep_config *cfg, int64_t *rows) {
+  if (rows == nullptr) return EP_ERR_INVALID_ARG;
+  const ep_status st = ep_validate_config(cfg);
+  if (st != EP_OK) return st;
+  *rows = ep::upper_bound(*cfg).rows;
+  return EP_OK;
+}
+
+ep_status ep_host_wait_flag(const volatile int32_t *flag, int32_t expected, int32_t timeout_ms) {
+  if (flag == nullptr || timeout_ms < 0) return EP_ERR_INVALID_ARG;
+  const auto deadline = std::chrono::steady_clock::now() + std::chrono::milliseconds(timeout_ms);
+  for (uint64_t spin = 0;; ++spin) {
+    if (__atomic_load_n(const_cast<const int32_t *>(flag), __ATOMIC_ACQUIRE) == expected)
+      return EP_OK;
+    if ((spin & 255) == 0 && std::chrono::steady_clock::now() >= deadline) return EP_ERR_TIMEOUT;
+    if (spin > 4096) std::this_thread::yield();
+  }
+}
+
+ep_status ep_layout(const ep_config *cfg, const void *topk_idx, ep_stream_t stream,
+                    ep_handle **out_handle, ep_layout_info *info) {
+  if (out_handle == nullptr || info == nullptr) return EP_ERR_INVALID_ARG;
+  *out_handle = nullptr;
+  ep_status st = ep_validate_config(cfg);
+  if (st != EP_OK) return st;
+  const ep_config c = *cfg;
+  const int T = c.num_tokens, K = c.num_topk, E = c.num_experts, R = c.num_ranks;
+  if (T > 0 && (topk_idx == nullptr || !aligned(topk_idx, c.topk_idx_is_int64 ? 8 : 4)))
+    return EP_ERR_INVALID_ARG;
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  if (c.do_cpu_sync) {
+    cudaStreamCaptureStatus cs = cudaStreamCaptureStatusNone;
+    if (cudaStreamIsCapturing(s, &cs) != cudaSuccess) return EP_ERR_CUDA;
+    if (cs != cudaStreamCaptureStatusNone) return EP_ERR_INVALID_ARG;
+  }
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return EP_ERR_CUDA;
+
+  const ep::Bounds b = ep::upper_bound(c);
+  ep::LayoutParams lp{};
+  lp.topk_idx = topk_idx;
+  lp.idx_is_int64 = c.topk_idx_is_int64;
+  lp.T = T; lp.K = K; lp.E = E; lp.R = R; lp.L = E / R;
+  lp.M = c.num_max_tokens_per_rank;
+  lp.A = c.expert_alignment;
+  lp.do_expand = c.do_expand;
+  // exact mode: rows never exceed the global bound; upper-bound mode: rows
+  // past the allocation are dropped and flagged
+  lp.row_limit = c.do_cpu_sync ? b.global : b.rows;
+  // Chunks of up to 256 tokens that never straddle a source rank.
+  lp.chunk_tokens = ep::kLayoutChunkTokens;
+  const int TB = lp.chunk_tokens;
+  const int64_t src_ranks = ((int64_t)T + lp.M - 1) / lp.M;
+  const int64_t max_tok = std::min<int64_t>(lp.M, T);
+  lp.blocks_per_src = (int)std::max<int64_t>(1, (max_tok + TB - 1) / TB);
+  const int64_t nblocks = std::max<int64_t>(1, src_ranks * lp.blocks_per_src);
+  if (nblocks > 0x7fffffff) return EP_ERR_UNSUPPORTED;
+  lp.num_blocks = (int)nblocks;
+  lp.rank_warps = ep::layout_rank_warps(c.do_expand ? E : R);
+  if (ep::layout_assign_smem(lp) > 220 * 1024) return EP_ERR_UNSUPPORTED;
+
+  // One device block, carved into 256-byte aligned arrays.
+  size_t off = 0;
+  auto take = [&](size_t bytes) {
+    const size_t o = off;
+    off += (bytes + 255) / 256 * 256;
+    return o;
+  };
+  const size_t o_ctrl = take(sizeof(int32_t) * ep::kCtrlWords);
+  const size_t o_topk = take(sizeof(int32_t) * (size_t)T * K);
+  const size_t o_dst = take(sizeof(int32_t) * (size_t)T * K);
+  const size_t o_meta = take(sizeof(int32_t) * 2 * (size_t)lp.row_limit);
+  const size_t o_inr = take((size_t)T * R);
+  const size_t o_cnte = take(sizeof(int32_t) * E);
+  const size_t o_cntea = take(sizeof(int32_t) * E);
+  const size_t o_pse = take(sizeof(int32_t) * (E + 1));
+  const size_t o_psp = take(sizeof(int32_t) * (E + 1));
+  const size_t o_cntr = take(sizeof(int32_t) * R);
+  const size_t o_psr = take(sizeof(int32_t) * (R + 1));
+  const size_t o_psrs = take(sizeof(int32_t) * (size_t)R * (R + 1));
+  const size_t o_blke = take(sizeof(int32_t) * (size_t)E * lp.num_blocks);
+  const size_t o_blkr = take(sizeof(int32_t) * (size_t)R * lp.num_blocks);
+  const size_t o_blkerr = take(sizeof(uint32_t) * (size_t)lp.num_blocks);
+  const size_t o_toks = take(c.use_fp8 ? sizeof(float) * (size_t)T * (c.hidden / ep::kFp8Block) : 0);
+  void *dmem = nullptr;
+  cudaMemPool_t pool = nullptr;
+  cudaError_t ce = ep::handle_pool(dev, &pool);
+  if (ce != cudaSuccess) return ep::cuda_status(ce);
+  ce = cudaMallocFromPoolAsync(&dmem, off, pool, s);
+  if (ce != cudaSuccess) return ep::cuda_status(ce);
+  uint8_t *base = static_cast<uint8_t *>(dmem);
+  lp.ctrl = reinterpret_cast<int32_t *>(base + o_ctrl);
+  lp.topk32 = reinterpret_cast<int32_t *>(base + o_topk);
+  lp.dst = reinterpret_cast<int32_t *>(base + o_dst);
+  lp.meta = reinterpret_cast<int32_t *>(base + o_meta);
+  lp.in_rank = base + o_inr;
+  lp.cnt_e = reinterpret_cast<int32_t *>(base + o_cnte);
+  lp.cnt_e_al = reinterpret_cast<int32_t *>(base + o_cntea);
+  lp.psum_e = reinterpret_cast<int32_t *>(base + o_pse);
+  lp.psum_pad = reinterpret_cast<int32_t *>(base + o_psp);
+  lp.cnt_r = reinterpret_cast<int32_t *>(base + o_cntr);
+  lp.psum_r = reinterpret_cast<int32_t *>(base + o_psr);
+  lp.psum_rs = reinterpret_cast<int32_t *>(base + o_psrs);
+  lp.blk_e = reinterpret_cast<int32_t *>(base + o_blke);
+  lp.blk_r = reinterpret_cast<int32_t *>(base + o_blkr);
+  lp.blk_err = reinterpret_cast<uint32_t *>(base + o_blkerr);
+  float *tok_scale = c.use_fp8 ? reinterpret_cast<float *>(base + o_toks) : nullptr;
+
+  auto fail = [&](ep_status code) {
+    cudaFreeAsync(dmem, s);
+    return code;
+  };
+
+  ep::HostSync *slot = nullptr;
+  if (c.do_cpu_sync) {
+    int32_t seq = 0;
+    slot = ep::sync_pool().acquire(&seq);
+    if (slot == nullptr) return fail(EP_ERR_OOM);
+    slot->flag = 0;
+    void *dptr = nullptr;
+    ce = cudaHostGetDevicePointer(&dptr, (void *)slot, 0);
+    if (ce != cudaSuccess) {
+      ep::sync_pool().release(slot);
+      return fail(ep::cuda_status(ce));
+    }
+    lp.host = static_cast<ep::HostSync *>(dptr);
+    lp.seq = seq;
+  }
+  ce = ep::launch_layout(lp, s);
+  if (ce != cudaSuccess) {
+    // the kernel may not have run: the slot is not safe to hand out again
+    return fail(ep::cuda_status(ce));
+  }
+
+  ep_handle *h = new ep_handle();
+  h->cfg = c;
+  h->device = dev;
+  h->stream = s;
+  h->dmem = dmem;
+  h->lp = lp;
+  h->lp.host = nullptr;
+  h->lp.topk_idx = nullptr;
+  h->tok_scale = tok_scale;
+
+  st = EP_OK;
+  int64_t num_recv = -1, num_exp = -1;
+  if (c.do_cpu_sync) {
+    const int32_t timeout = c.cpu_sync_timeout_ms > 0 ? c.cpu_sync_timeout_ms : 10000;
+    const ep_status w = ep_host_wait_flag(&slot->flag, lp.seq, timeout);
+    if (w != EP_OK) {
+      // the slot may still be written later: leave it out of the pool
+      delete h;
+      return fail(w);
+    }
+    const int32_t err = slot->error;
+    num_recv = slot->num_recv;
+    num_exp = slot->num_expanded;
+    ep::sync_pool().release(slot);
+    h->rows_alloc = c.do_expand ? num_exp : num_recv;
+    if (err & EP_ERRBIT_BAD_TOPK_IDX) st = EP_ERR_BAD_TOPK_IDX;
+  } else {
+    h->rows_alloc = b.rows;
+  }
+  const int64_t nb = c.hidden / ep::kFp8Block;
+  if (c.use_fp8) {
+    if (c.use_tma_aligned_col_major_sf) {
+      h->sf_token_stride = 1;
+      h->sf_hidden_stride = align_up(h->rows_alloc, 4);
+      h->sf_numel = nb * h->sf_hidden_stride;
+    } else {
+      h->sf_token_stride = nb;
+      h->sf_hidden_stride = 1;
+      h->sf_numel = nb * h->rows_alloc;
+    }
+  } else {
+    h->sf_token_stride = h->sf_hidden_stride = h->sf_numel = 0;
+  }
+
+  info->num_recv_tokens = num_recv;
+  info->num_expanded_tokens = num_exp;
+  info->rows_alloc = h->rows_alloc;
+  info->sf_numel = h->sf_numel;
+  info->sf_token_stride = h->sf_token_stride;
+  info->sf_hidden_stride = h->sf_hidden_stride;
+  info->topk_idx = lp.topk32;
+  info->cnt_expert = lp.cnt_e;
+  info->cnt_expert_aligned = lp.cnt_e_al;
+  info->psum_expert = lp.psum_e;
+  info->cnt_rank = lp.cnt_r;
+  info->psum_rank = lp.psum_r;
+  info->psum_rank_src = lp.psum_rs;
+  info->dst_buffer_slot_idx = lp.dst;
+  info->recv_src_metadata = lp.meta;
+  info->is_token_in_rank = lp.in_rank;
+  info->totals = lp.ctrl + ep::kCtrlNumRecv;
+  info->error_word = reinterpret_cast<const uint32_t *>(lp.ctrl + ep::kCtrlError);
+  info->meta_rows = lp.row_limit;
+  *out_handle = h;
+  return st;
+}
+
+ep_status ep_dispatch(ep_handle *h, const void *x, const float *topk_weights, void *recv_x,
+                      float *recv_sf, float *recv_topk_weights, int32_t *recv_topk_idx,
+                      ep_stream_t stream) {
+  if (h == nullptr) return EP_ERR_INVALID_ARG;
+  const ep_config &c = h->cfg;
+  const int T = c.num_tokens;
+  if (T > 0 && (x == nullptr || !aligned(x, 16))) return EP_ERR_INVALID_ARG;
+  if (h->rows_alloc > 0 && (recv_x == nullptr || !aligned(recv_x, 16))) return EP_ERR_INVALID_ARG;
+  if (c.use_fp8) {
+    if (h->rows_alloc > 0 && (recv_sf == nullptr || !aligned(recv_sf, 4))) return EP_ERR_INVALID_ARG;
+  } else if (recv_sf != nullptr) {
+    return EP_ERR_INVALID_ARG;
+  }
+  if (recv_topk_weights != nullptr && (topk_weights == nullptr || !aligned(recv_topk_weights, 4)))
+    return EP_ERR_INVALID_ARG;
+  if (topk_weights != nullptr && !aligned(topk_weights, 4)) return EP_ERR_INVALID_ARG;
+  if (recv_topk_idx != nullptr && (c.do_expand || !aligned(recv_topk_idx, 4)))
+    return EP_ERR_INVALID_ARG;
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return EP_ERR_CUDA;
+  if (dev != h->device) return EP_ERR_INVALID_ARG;
+
+  ep::DispatchParams p{};
+  p.x = static_cast<const uint16_t *>(x);
+  p.topk_w = topk_weights;
+  p.topk32 = h->lp.topk32;
+  p.dst = h->lp.dst;
+  p.psum_e = h->lp.psum_e;
+  p.cnt_e = h->lp.cnt_e;
+  p.psum_pad = h->lp.psum_pad;
+  p.T = T;
+  p.K = c.num_topk;
+  p.E = c.num_experts;
+  p.L = c.num_experts / c.num_ranks;
+  p.H = c.hidden;
+  p.do_expand = c.do_expand;
+  p.zero_padding = c.do_expand && c.do_zero_padding;
+  p.max_pad_items = c.do_expand ? ((int64_t)c.num_experts * (c.expert_alignment - 1) + 7) / 8 : 0;
+  p.rows_alloc = h->rows_alloc;
+  p.sf_hidden_stride = h->sf_hidden_stride;
+  p.sf_token_stride = h->sf_token_stride;
+  p.recv_x = recv_x;
+  p.recv_sf = recv_sf;
+  p.recv_w = recv_topk_weights;
+  p.recv_idx = recv_topk_idx;
+  p.err = reinterpret_cast<unsigned *>(h->lp.ctrl + ep::kCtrlError);
+  p.tok_scale = h->tok_scale;
+  p.meta = h->lp.meta;
+  p.num_rows = h->lp.ctrl + (c.do_expand ? ep::kCtrlNumExpanded : ep::kCtrlNumRecv);
+  if (h->rows_alloc == 0) return EP_OK;  // nothing lands anywhere
+  const cudaError_t ce =
+      ep::launch_dispatch(p, c.use_fp8, c.use_tma_aligned_col_major_sf, c.num_sms,
+                          reinterpret_cast<cudaStream_t>(stream));
+  return ep::cuda_status(ce);
+}
+
+ep_status ep_combine(const ep_handle *h, const void *y, const float *topk_weights,
+                     const void *bias_0, const void *bias_1, const void *expert_bias, void *out,
+                     ep_stream_t stream) {
+  if (h == nullptr) return EP_ERR_INVALID_ARG;
+  const ep_config &c = h->cfg;
+  const int T = c.num_tokens;
+  if (T > 0 && (out == nullptr || !aligned(out, 16))) return EP_ERR_INVALID_ARG;
+  if (h->rows_alloc > 0 && (y == nullptr || !aligned(y, 16))) return EP_ERR_INVALID_ARG;
+  if (topk_weights != nullptr && !aligned(topk_weights, 4)) return EP_ERR_INVALID_ARG;
+  if ((bias_0 != nullptr && !aligned(bias_0, 16)) || (bias_1 != nullptr && !aligned(bias_1, 16)) ||
+      (expert_bias != nullptr && !aligned(expert_bias, 16)))
+    return EP_ERR_INVALID_ARG;
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return EP_ERR_CUDA;
+  if (dev != h->device) return EP_ERR_INVALID_ARG;
+  ep::CombineParams p{};
+  p.y = static_cast<const uint16_t *>(y);
+  p.topk_w = topk_weights;
+  p.topk32 = h->lp.topk32;
+  p.dst = h->lp.dst;
+  p.bias0 = static_cast<const uint16_t *>(bias_0);
+  p.bias1 = static_cast<const uint16_t *>(bias_1);
+  p.ebias = static_cast<const uint16_t *>(expert_bias);
+  p.out = static_cast<uint16_t *>(out);
+  p.err = reinterpret_cast<unsigned *>(h->lp.ctrl + ep::kCtrlError);
+  p.T = T;
+  p.K = c.num_topk;
+  p.H = c.hidden;
+  p.rows_alloc = h->rows_alloc;
+  const cudaError_t ce = ep::launch_combine(p, c.num_sms, reinterpret_cast<cudaStream_t>(stream));
+  return ep::cuda_status(ce);
+}
+
+void ep_handle_free(ep_handle *h) {
+  if (h == nullptr) return;
+  int cur = -1;
+  cudaGetDevice(&cur);
+  if (cur != h->device) cudaSetDevice(h->device);
+  if (cudaFreeAsync(h->dmem, h->stream) != cudaSuccess) {
+    cudaGetLastError();  // e.g. the layout stream was destroyed: free synchronously
+    cudaFree(h->dmem);
+  }
+  if (cur >= 0 && cur != h->device) cudaSetDevice(cur);
+  delete h;
+}
+
+}  // extern "C"

@@ -1,0 +1,271 @@
+// Combine: per-token weighted gather-reduce of expert outputs, fp32 -> BF16.
+//
+// Follows "DeepEP V2 notes, ch. 8: combine, handle and async overlap", §8.1
+// (combine walks the dispatch handle backwards, with optional bias and top-k
+// weights) and the vLLM PR #52781 review (combine takes BF16 expert output;
+// with topk_weights = None the caller has already applied the weights).
+//
+// Work unit = (token, chunk of the hidden dimension).  Persistent CTAs, warp
+// specialised:
+//   warp 0 (producer) reads a unit's routing (destination rows, weights,
+//     expert ids; prefetched one unit ahead), compacts the valid slots
+//     (dropping repeated rows when there are no weights) and issues one
+//     cp.async.bulk global->shared copy per slot row chunk (plus the expert-
+//     bias and per-token bias chunks) into a ring of kStages shared-memory
+//     stages, completion counted on the stage's "full" mbarrier;
+//   the other warps (consumers) wait for a stage, accumulate its rows
+//     strictly in slot order with separately rounded fp32 multiplies and adds
+//     (__fmul_rn / __fadd_rn: no FMA contraction), add the biases, round to
+//     BF16 (nearest even), store the output chunk, and release the stage on
+//     its "empty" mbarrier.
+// Each output element is written by exactly one thread: no atomics.  Every
+// mbarrier wait is bounded; a wait that gives up sets EP_ERRBIT_TIMEOUT in
+// the handle's error word and the CTA returns.
+#include <algorithm>
+
+#include "ep_internal.cuh"
+#include "ep_ptx.cuh"
+
+namespace ep {
+namespace {
+
+constexpr int kStages = 3;
+constexpr int kMaxConsumers = 224;
+constexpr int kWaitIters = 4000;          // x kWaitHintNs: gives up after ~2 s
+constexpr uint32_t kWaitHintNs = 500000;
+
+struct StageMeta {
+  float w[EP_MAX_TOPK];
+  int n;      // valid slots in this unit
+};
+
+__device__ __forceinline__ void unpack8(const uint4 &v, float *f) {
+  f[0] = bf16_lo(v.x); f[1] = bf16_hi(v.x);
+  f[2] = bf16_lo(v.y); f[3] = bf16_hi(v.y);
+  f[4] = bf16_lo(v.z); f[5] = bf16_hi(v.z);
+  f[6] = bf16_lo(v.w); f[7] = bf16_hi(v.w);
+}
+
+struct Routing {
+  int d, e;
+  float w;
+};
+
+template <bool HAS_W, bool HAS_EB>
+__device__ __forceinline__ Routing load_routing(const CombineParams &p, int64_t unit, int nchunks,
+                                                int lane) {
+  Routing r{-1, -1, 1.f};
+  const int64_t t = unit / nchunks;
+  if (lane < p.K) {
+    r.d = __ldg(p.dst + t * p.K + lane);
+    if (HAS_EB) r.e = __ldg(p.topk32 + t * p.K + lane);
+    if (HAS_W) r.w = __ldg(p.topk_w + t * p.K + lane);
+  }
+  return r;
+}
+
+template <bool HAS_W, bool HAS_EB>
+__global__ void __launch_bounds__(kMaxConsumers + 32, 1)
+    combine_kernel(CombineParams p, int chunk_bytes, int nchunks, int slots_cap) {
+  extern __shared__ __align__(128) uint8_t smem[];
+  __shared__ __align__(8) uint64_t full[kStages];
+  __shared__ __align__(8) uint64_t empty[kStages];
+  __shared__ StageMeta meta[kStages];
+
+  const int H = p.H;
+  const int64_t row_bytes = 2 * (int64_t)H;
+  const int64_t stage_bytes = (int64_t)slots_cap * chunk_bytes;
+  const int64_t num_units = (int64_t)p.T * nchunks;
+  const int has_b0 = p.bias0 != nullptr, has_b1 = p.bias1 != nullptr;
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  const int ncw = (blockDim.x >> 5) - 1;  // consumer warps
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < kStages; ++s) {
+      mbar_init(&full[s], 1);
+      mbar_init(&empty[s], ncw);
+    }
+    fence_mbar_init();
+  }
+  __syncthreads();
+
+  if (warp == 0) {
+    // ---------------- producer ----------------
+    const uint64_t stream_pol = l2_policy_evict_first();  // expert outputs are read once
+    // routing of the next four units is in flight while one is issued
+    int64_t u = blockIdx.x;
+    const int64_t G = gridDim.x;
+    Routing r0{-1, -1, 1.f}, r1{-1, -1, 1.f}, r2{-1, -1, 1.f}, r3{-1, -1, 1.f};
+    if (u < num_units) r0 = load_routing<HAS_W, HAS_EB>(p, u, nchunks, lane);
+    if (u + G < num_units) r1 = load_routing<HAS_W, HAS_EB>(p, u + G, nchunks, lane);
+    if (u + 2 * G < num_units) r2 = load_routing<HAS_W, HAS_EB>(p, u + 2 * G, nchunks, lane);
+    if (u + 3 * G < num_units) r3 = load_routing<HAS_W, HAS_EB>(p, u + 3 * G, nchunks, lane);
+    for (int64_t i = 0; u < num_units; ++i, u += G) {
+      const Routing cur = r0;
+      r0 = r1;
+      r1 = r2;
+      r2 = r3;
+      if (u + 4 * G < num_units) r3 = load_routing<HAS_W, HAS_EB>(p, u + 4 * G, nchunks, lane);
+      const int s = (int)(i % kStages);
+      const int64_t k = i / kStages;
+      if (k > 0) {
+        bool ok = false;
+        if (lane == 0) ok = mbar_wait_bounded(&empty[s], (uint32_t)((k - 1) & 1), kWaitIters,
+                                              kWaitHintNs);
+        ok = __shfl_sync(0xffffffffu, ok, 0);
+        if (!ok) {
+          if (lane == 0) atomicOr(p.err, EP_ERRBIT_TIMEOUT);
+          return;
+        }
+      }
+      const int64_t t = u / nchunks;
+      const int64_t off = (u - t * nchunks) * (int64_t)chunk_bytes;
+      const uint32_t bytes = (uint32_t)min((int64_t)chunk_bytes, row_bytes - off);
+      bool use = cur.d >= 0;
+      if (!HAS_W) {  // weights already applied: each row counts once
+        const unsigned peers = __match_any_sync(0xffffffffu, cur.d);
+        use = use && lane == __ffs(peers) - 1;
+      }
+      const unsigned m = __ballot_sync(0xffffffffu, use);
+      const int n = __popc(m);
+      const int pos = __popc(m & lanemask_lt());
+      if (use) meta[s].w[pos] = cur.w;
+      if (lane == 0) meta[s].n = n;
+      __syncwarp();
+      const int rows = n * (HAS_EB ? 2 : 1) + has_b0 + has_b1;
+      if (lane == 0) {
+        if (rows > 0)
+          mbar_arrive_expect_tx(&full[s], (uint32_t)rows * bytes);
+        else
+          mbar_arrive(&full[s]);
+      }
+      __syncwarp();
+      uint8_t *sb = smem + s * stage_bytes;
+      if (use) {
+        bulk_load_g2s_hint(sb + (int64_t)pos * chunk_bytes,
+                           reinterpret_cast<const uint8_t *>(p.y) + (int64_t)cur.d * row_bytes + off,
+                           bytes, &full[s], stream_pol);
+        if (HAS_EB)
+          bulk_load_g2s(sb + (int64_t)(n + pos) * chunk_bytes,
+                        reinterpret_cast<const uint8_t *>(p.ebias) + (int64_t)cur.e * row_bytes + off,
+                        bytes, &full[s]);
+      }
+      const int brow = n * (HAS_EB ? 2 : 1);
+      if (lane == 0 && has_b0)
+        bulk_load_g2s(sb + (int64_t)brow * chunk_bytes,
+                      reinterpret_cast<const uint8_t *>(p.bias0) + t * row_bytes + off, bytes,
+                      &full[s]);
+      if (lane == 1 && has_b1)
+        bulk_load_g2s(sb + (int64_t)(brow + has_b0) * chunk_bytes,
+                      reinterpret_cast<const uint8_t *>(p.bias1) + t * row_bytes + off, bytes,
+                      &full[s]);
+    }
+    return;
+  }
+
+  // ---------------- consumers ----------------
+  const int ctid = threadIdx.x - 32;
+  const int cthreads = blockDim.x - 32;
+  int64_t i = 0;
+  for (int64_t u = blockIdx.x; u < num_units; u += gridDim.x, ++i) {
+    const int s = (int)(i % kStages);
+    const uint32_t par = (uint32_t)((i / kStages) & 1);
+    if (!mbar_wait_bounded(&full[s], par, kWaitIters, kWaitHintNs)) {
+      if (lane == 0) atomicOr(p.err, EP_ERRBIT_TIMEOUT);
+      return;
+    }
+    const int64_t t = u / nchunks;
+    const int64_t off = (u - t * nchunks) * (int64_t)chunk_bytes;
+    const int nv = (int)(min((int64_t)chunk_bytes, row_bytes - off) / 16);
+    const int n = meta[s].n;
+    const uint8_t *sb = smem + s * stage_bytes;
+    for (int v = ctid; v < nv; v += cthreads) {
+      float acc[8];
+#pragma unroll
+      for (int q = 0; q < 8; ++q) acc[q] = 0.f;
+      for (int j = 0; j < n; ++j) {
+        float f[8];
+        unpack8(*reinterpret_cast<const uint4 *>(sb + (int64_t)j * chunk_bytes + v * 16), f);
+        if (HAS_EB) {
+          float b[8];
+          unpack8(*reinterpret_cast<const uint4 *>(sb + (int64_t)(n + j) * chunk_bytes + v * 16), b);
+#pragma unroll
+          for (int q = 0; q < 8; ++q) f[q] = __fadd_rn(f[q], b[q]);
+        }
+        if (HAS_W) {
+          const float w = meta[s].w[j];
+#pragma unroll
+          for (int q = 0; q < 8; ++q) acc[q] = __fadd_rn(acc[q], __fmul_rn(w, f[q]));
+        } else {
+#pragma unroll
+          for (int q = 0; q < 8; ++q) acc[q] = __fadd_rn(acc[q], f[q]);
+        }
+      }
+      const int brow = n * (HAS_EB ? 2 : 1);
+      for (int b = 0; b < has_b0 + has_b1; ++b) {
+        float f[8];
+        unpack8(*reinterpret_cast<const uint4 *>(sb + (int64_t)(brow + b) * chunk_bytes + v * 16), f);
+#pragma unroll
+        for (int q = 0; q < 8; ++q) acc[q] = __fadd_rn(acc[q], f[q]);
+      }
+      uint4 o;
+      o.x = cvt_bf16x2(acc[0], acc[1]);
+      o.y = cvt_bf16x2(acc[2], acc[3]);
+      o.z = cvt_bf16x2(acc[4], acc[5]);
+      o.w = cvt_bf16x2(acc[6], acc[7]);
+      st_stream_v4(reinterpret_cast<uint8_t *>(p.out) + t * row_bytes + off + (int64_t)v * 16, o);
+    }
+    __syncwarp();
+    if (lane == 0) mbar_arrive(&empty[s]);
+  }
+}
+
+template <bool W, bool EB>
+cudaError_t launch_one(const CombineParams &p, int sm_cap, cudaStream_t s) {
+  auto kern = combine_kernel<W, EB>;
+  const int64_t row_bytes = 2 * (int64_t)p.H;
+  const int nbias = (p.bias0 != nullptr) + (p.bias1 != nullptr);
+  const int slots_cap = p.K * (EB ? 2 : 1) + nbias;
+  // Stage budget ~96 KB per CTA (two CTAs per SM); chunks are equal-sized
+  // multiples of 16 bytes.
+  const int64_t budget = 96 * 1024 / kStages;
+  int64_t chunk = std::max<int64_t>(16, budget / slots_cap / 16 * 16);
+  chunk = std::min(chunk, row_bytes);
+  const int nchunks = (int)((row_bytes + chunk - 1) / chunk);
+  chunk = ((row_bytes + nchunks - 1) / nchunks + 15) / 16 * 16;
+  const int nv = (int)(chunk / 16);
+  const int consumers = std::min(kMaxConsumers, (nv + 31) / 32 * 32);
+  const int threads = consumers + 32;
+  const size_t smem = (size_t)kStages * slots_cap * chunk;
+  cudaError_t err;
+  if (smem > 48 * 1024) {
+    err = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    if (err != cudaSuccess) return err;
+  }
+  int dev = 0;
+  err = cudaGetDevice(&dev);
+  if (err != cudaSuccess) return err;
+  int per_sm = 0;
+  err = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kern, threads, smem);
+  if (err != cudaSuccess) return err;
+  if (per_sm < 1) per_sm = 1;
+  const int sms = device_sm_count(dev);
+  const int use_sms = (sm_cap > 0 && sm_cap < sms) ? sm_cap : sms;
+  const int64_t units = (int64_t)p.T * nchunks;
+  const int64_t grid = std::min<int64_t>((int64_t)use_sms * per_sm, units);
+  if (grid <= 0) return cudaSuccess;
+  kern<<<(int)grid, threads, smem, s>>>(p, (int)chunk, nchunks, slots_cap);
+  return cudaGetLastError();
+}
+
+}  // namespace
+
+cudaError_t launch_combine(const CombineParams &p, int sm_cap, cudaStream_t s) {
+  const bool w = p.topk_w != nullptr, eb = p.ebias != nullptr;
+  if (w && eb) return launch_one<true, true>(p, sm_cap, s);
+  if (w) return launch_one<true, false>(p, sm_cap, s);
+  if (eb) return launch_one<false, true>(p, sm_cap, s);
+  return launch_one<false, false>(p, sm_cap, s);
+}
+
+}  // namespace ep

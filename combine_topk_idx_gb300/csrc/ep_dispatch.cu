@@ -1,0 +1,393 @@
+// Dispatch copy epilogue: source rows -> rank layout or expert-expanded layout.
+//
+// Follows "DeepEP V2 notes, ch. 7: how V2 dispatch builds expert inputs",
+// §7.3 (copy epilogue: expand / rank layout, expert_alignment padding,
+// do_zero_padding, TMA-aligned column-major scale factors) and §7.4; the FP8
+// payload is e4m3 with one fp32 scale per 1x128 block (scale = amax / 448).
+//
+// Token-major scatter with persistent, warp-specialised CTAs:
+//   warp 0 (producer) takes the CTA's tokens in turn, reads each token's K
+//     destination rows (prefetched one token ahead), keeps the distinct ones
+//     (rank-layout slots of one rank share a row), writes the per-row weights
+//     and local expert ids, and issues one cp.async.bulk global->shared copy
+//     of the token's BF16 row into a ring of kStages input stages;
+//   the consumer warps wait for a stage and
+//     FP8:  quantise it -- amax of each 128-element block by a 16-lane
+//           shuffle, scale = amax / 448 and x / scale with IEEE divisions,
+//           packed cvt.rn.satfinite.e4m3x2 -- into an output stage, then one
+//           thread issues one cp.async.bulk shared->global store per distinct
+//           destination row while the others write the scales;
+//     BF16: one thread stores the input stage itself to every row.
+// The source row is read from HBM once and quantised once whatever K is; the
+// TMA engine moves every payload byte.  After the tokens, the consumer warps
+// zero the alignment padding rows in 8-row work items.  Every mbarrier wait
+// is bounded: a wait that gives up sets EP_ERRBIT_TIMEOUT and the CTA returns.
+#include <algorithm>
+
+#include "ep_internal.cuh"
+#include "ep_ptx.cuh"
+
+namespace ep {
+namespace {
+
+constexpr int kStages = 3;
+constexpr int kPadRowsPerItem = 8;
+constexpr int kMaxConsumers = 224;
+constexpr int kWaitIters = 4000;          // x kWaitHintNs: gives up after ~2 s
+constexpr uint32_t kWaitHintNs = 500000;
+constexpr int kBarConsumers = 1;          // named barrier id (0 is __syncthreads)
+
+struct TokenMeta {
+  int rows[EP_MAX_TOPK];
+  int n;
+};
+
+// Expert whose padding range holds padding row q: the last e with psum_pad[e] <= q.
+__device__ __forceinline__ int padding_expert(const int32_t *psum_pad, int E, int q) {
+  int lo = 0, hi = E;
+  while (lo < hi) {
+    const int mid = (lo + hi + 1) >> 1;
+    if (__ldg(psum_pad + mid) <= q) lo = mid; else hi = mid - 1;
+  }
+  return lo;
+}
+
+// One work item of alignment padding: up to kPadRowsPerItem consecutive
+// padding rows (numbered across all experts): zero payload, scales, weight.
+// Run by the consumer threads only (ctid in [0, nct)).
+__device__ __forceinline__ void zero_padding_item(const DispatchParams &p, int item, int npad,
+                                                  int *prow, bool fp8, bool col_major, int ctid,
+                                                  int nct) {
+  const int q0 = item * kPadRowsPerItem;
+  if (ctid < kPadRowsPerItem) {
+    const int q = q0 + ctid;
+    int64_t row = -1;
+    if (q < npad) {
+      const int e = padding_expert(p.psum_pad, p.E, q);
+      row = (int64_t)__ldg(p.psum_e + e) + __ldg(p.cnt_e + e) + (q - __ldg(p.psum_pad + e));
+      if (row >= p.rows_alloc) row = -1;
+    }
+    prow[ctid] = (int)row;
+  }
+  named_barrier(kBarConsumers, nct);
+  if (p.recv_w != nullptr && ctid < kPadRowsPerItem && prow[ctid] >= 0) p.recv_w[prow[ctid]] = 0.f;
+  if (!p.zero_padding) return;
+  const int64_t row_bytes = fp8 ? p.H : 2 * (int64_t)p.H;
+  const int n16 = (int)(row_bytes / 16);
+  const uint4 z = make_uint4(0, 0, 0, 0);
+  uint8_t *recv = static_cast<uint8_t *>(p.recv_x);
+  for (int i = ctid; i < kPadRowsPerItem * n16; i += nct) {
+    const int r = i / n16;
+    const int row = prow[r];
+    if (row >= 0) st_stream_v4(recv + (int64_t)row * row_bytes + (int64_t)(i - r * n16) * 16, z);
+  }
+  if (fp8 && !col_major) {  // column-major padding scales are zeroed by the scale gather
+    const int nb = p.H / kFp8Block;
+    for (int i = ctid; i < kPadRowsPerItem * nb; i += nct) {
+      const int r = i / nb;
+      const int row = prow[r];
+      if (row >= 0) p.recv_sf[(int64_t)row * nb + (i - r * nb)] = 0.f;
+    }
+  }
+}
+
+struct Routing {
+  int d, e;
+  float w;
+};
+
+__device__ __forceinline__ Routing load_routing(const DispatchParams &p, int t, int lane) {
+  Routing r{-1, -1, 0.f};
+  if (lane < p.K) {
+    const int64_t o = (int64_t)t * p.K + lane;
+    r.d = __ldg(p.dst + o);
+    r.e = __ldg(p.topk32 + o);
+    if (p.topk_w != nullptr) r.w = __ldg(p.topk_w + o);
+  }
+  return r;
+}
+
+template <bool FP8, bool COL_MAJOR>
+__global__ void __launch_bounds__(kMaxConsumers + 32, 1) dispatch_kernel(DispatchParams p) {
+  extern __shared__ __align__(128) uint8_t smem[];
+  __shared__ __align__(8) uint64_t full[kStages];
+  __shared__ __align__(8) uint64_t empty[kStages];
+  __shared__ TokenMeta meta[kStages];
+  __shared__ int prow_s[2][kPadRowsPerItem];
+
+  const int H = p.H;
+  const int in_bytes = 2 * H;                              // BF16 source row
+  const int in_stage = (in_bytes + 127) / 128 * 128;
+  const int out_bytes = FP8 ? H : 2 * H;                   // destination row
+  const int out_stage = FP8 ? (H + 127) / 128 * 128 : 0;
+  const int nb = H / kFp8Block;
+  const int nb_pad = (nb + 31) / 32 * 32;
+  uint8_t *in0 = smem;
+  uint8_t *out0 = smem + kStages * in_stage;
+  float *sf0 = reinterpret_cast<float *>(out0 + kStages * out_stage);  // row-major scales
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  const int ncw = (blockDim.x >> 5) - 1;
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < kStages; ++s) {
+      mbar_init(&full[s], 1);
+      mbar_init(&empty[s], ncw);
+    }
+    fence_mbar_init();
+  }
+  __syncthreads();
+
+  // x rows and the destination payload are touched once: evict them first so
+  // that the small, scattered scale-factor sectors stay in L2 until complete.
+  const uint64_t stream_pol = l2_policy_evict_first();
+  if (warp == 0) {
+    // ---------------- producer ----------------
+    // routing of the next kPrefetch tokens is in flight while one is issued
+    int t = blockIdx.x;
+    const int G = gridDim.x;
+    Routing r0{-1, -1, 0.f}, r1{-1, -1, 0.f}, r2{-1, -1, 0.f}, r3{-1, -1, 0.f};
+    if (t < p.T) r0 = load_routing(p, t, lane);
+    if (t + G < p.T) r1 = load_routing(p, t + G, lane);
+    if (t + 2 * G < p.T) r2 = load_routing(p, t + 2 * G, lane);
+    if (t + 3 * G < p.T) r3 = load_routing(p, t + 3 * G, lane);
+    for (int64_t i = 0; t < p.T; ++i, t += G) {
+      const Routing cur = r0;
+      r0 = r1;
+      r1 = r2;
+      r2 = r3;
+      if (t + 4 * (int64_t)G < p.T) r3 = load_routing(p, t + 4 * G, lane);
+      const int s = (int)(i % kStages);
+      const int64_t k = i / kStages;
+      if (k > 0) {
+        bool ok = false;
+        if (lane == 0)
+          ok = mbar_wait_bounded(&empty[s], (uint32_t)((k - 1) & 1), kWaitIters, kWaitHintNs);
+        ok = __shfl_sync(0xffffffffu, ok, 0);
+        if (!ok) {
+          if (lane == 0) atomicOr(p.err, EP_ERRBIT_TIMEOUT);
+          return;
+        }
+      }
+      const unsigned peers = __match_any_sync(0xffffffffu, cur.d);
+      const bool keep = cur.d >= 0 && lane == __ffs(peers) - 1;
+      const unsigned keepm = __ballot_sync(0xffffffffu, keep);
+      const int n = __popc(keepm);
+      if (keep) meta[s].rows[__popc(keepm & lanemask_lt())] = cur.d;
+      if (lane == 0) meta[s].n = n;
+      if (p.do_expand) {
+        if (keep && p.recv_w != nullptr) p.recv_w[cur.d] = cur.w;
+      } else if (p.recv_w != nullptr || p.recv_idx != nullptr) {
+        const int rk = keep ? cur.e / p.L : -1;
+        for (int kk = 0; kk < p.K; ++kk) {
+          const int ek = __shfl_sync(0xffffffffu, cur.e, kk);
+          const float wk = __shfl_sync(0xffffffffu, cur.w, kk);
+          if (keep) {
+            const bool same = ek >= 0 && ek / p.L == rk;
+            const int64_t o = (int64_t)cur.d * p.K + kk;
+            if (p.recv_w != nullptr) p.recv_w[o] = same ? wk : 0.f;
+            if (p.recv_idx != nullptr) p.recv_idx[o] = same ? ek - rk * p.L : -1;
+          }
+        }
+      }
+      __syncwarp();
+      if (lane == 0) {
+        if (n > 0) {
+          mbar_arrive_expect_tx(&full[s], (uint32_t)in_bytes);
+          bulk_load_g2s_hint(in0 + s * in_stage, p.x + (int64_t)t * H, (uint32_t)in_bytes, &full[s],
+                             stream_pol);
+        } else {
+          mbar_arrive(&full[s]);
+        }
+      }
+    }
+    return;
+  }
+
+  // ---------------- consumers ----------------
+  const int ctid = threadIdx.x - 32;
+  const int nct = blockDim.x - 32;
+  const int nvec = H / 8;  // 16-byte vectors of the BF16 row
+  const bool pad_work = p.do_expand && (p.zero_padding || p.recv_w != nullptr);
+  const int npad = pad_work ? __ldg(p.psum_pad + p.E) : 0;
+  const int64_t num_items = (int64_t)p.T + (npad + kPadRowsPerItem - 1) / kPadRowsPerItem;
+  uint8_t *recv = static_cast<uint8_t *>(p.recv_x);
+  int64_t i = 0;
+  int pi = 0;
+  for (int64_t item = blockIdx.x; item < num_items; item += gridDim.x) {
+    if (item >= p.T) {  // every token item comes before the padding items
+      zero_padding_item(p, (int)(item - p.T), npad, prow_s[pi & 1], FP8, COL_MAJOR, ctid, nct);
+      ++pi;
+      continue;
+    }
+    const int s = (int)(i % kStages);
+    const uint32_t par = (uint32_t)((i / kStages) & 1);
+    ++i;
+    if (!mbar_wait_bounded(&full[s], par, kWaitIters, kWaitHintNs)) {
+      if (lane == 0) atomicOr(p.err, EP_ERRBIT_TIMEOUT);
+      if (ctid == 0) bulk_wait_all<0>();
+      return;
+    }
+    const int n = meta[s].n;
+    const int t = (int)item;
+    const uint8_t *in = in0 + s * in_stage;
+    if constexpr (FP8) {
+      uint8_t *out = out0 + s * out_stage;
+      float *sf = sf0 + s * nb_pad;
+      if (n > 0) {
+        if (ctid == 0) bulk_wait_read<kStages - 1>();  // out stage s no longer read
+        named_barrier(kBarConsumers, nct);
+        // every consumer thread runs the same number of iterations so the
+        // 16-lane shuffles always see full warps (nvec and nct are multiples of 16)
+        for (int v0 = 0; v0 < nvec; v0 += nct) {
+          const int v = v0 + ctid;
+          const bool valid = v < nvec;
+          const uint4 x8 = valid ? *reinterpret_cast<const uint4 *>(in + v * 16)
+                                 : make_uint4(0, 0, 0, 0);
+          float f[8];
+          f[0] = bf16_lo(x8.x); f[1] = bf16_hi(x8.x);
+          f[2] = bf16_lo(x8.y); f[3] = bf16_hi(x8.y);
+          f[4] = bf16_lo(x8.z); f[5] = bf16_hi(x8.z);
+          f[6] = bf16_lo(x8.w); f[7] = bf16_hi(x8.w);
+          float amax = 0.f;
+#pragma unroll
+          for (int q = 0; q < 8; ++q) amax = fmaxf(amax, fabsf(f[q]));
+          // 16 consecutive lanes hold one 128-element block
+          amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, 1));
+          amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, 2));
+          amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, 4));
+          amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, 8));
+          if (valid) {
+            const float sc = __fdiv_rn(amax, 448.0f);
+            uint2 packed = make_uint2(0, 0);
+            if (amax != 0.f) {
+              float g[8];
+#pragma unroll
+              for (int q = 0; q < 8; ++q) g[q] = __fdiv_rn(f[q], sc);
+              packed.x = cvt_e4m3x2(g[0], g[1]) | (cvt_e4m3x2(g[2], g[3]) << 16);
+              packed.y = cvt_e4m3x2(g[4], g[5]) | (cvt_e4m3x2(g[6], g[7]) << 16);
+            }
+            *reinterpret_cast<uint2 *>(out + v * 8) = packed;
+            if ((v & 15) == 0) {
+              if (COL_MAJOR)
+                p.tok_scale[(int64_t)t * nb + (v >> 4)] = sc;
+              else
+                sf[v >> 4] = sc;
+            }
+          }
+        }
+        fence_proxy_async_smem();
+        named_barrier(kBarConsumers, nct);
+        if (ctid == 0) {
+          for (int r = 0; r < n; ++r)
+            bulk_store_s2g_hint(recv + (int64_t)meta[s].rows[r] * out_bytes, out, (uint32_t)out_bytes,
+                                stream_pol);
+          bulk_commit();
+        }
+        if (!COL_MAJOR) {  // row-major scales: nb contiguous floats per row
+          for (int e = ctid; e < n * nb; e += nct) {
+            const int r = e / nb, j = e - r * nb;
+            p.recv_sf[(int64_t)meta[s].rows[r] * nb + j] = sf[j];
+          }
+        }
+      } else if (ctid == 0) {
+        bulk_commit();  // one (here empty) bulk group per token keeps the stage reuse count exact
+      }
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&empty[s]);
+    } else {
+      // BF16: the input stage is the payload; it is released once its bulk
+      // stores have read it.
+      if (ctid == 0) {
+        for (int r = 0; r < n; ++r)
+          bulk_store_s2g_hint(recv + (int64_t)meta[s].rows[r] * out_bytes, in, (uint32_t)out_bytes,
+                              stream_pol);
+        bulk_commit();
+        bulk_wait_read<0>();
+      }
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&empty[s]);
+    }
+  }
+  if (ctid == 0) bulk_wait_all<0>();
+}
+
+// Column-major scale factors of every destination row, gathered from the
+// per-token scales through the row's source token (recv_src_metadata).  One
+// thread per row: 16-byte loads of the token's scales, and for each scale
+// block j the warp writes 32 consecutive rows (coalesced).  Padding rows get 0.
+__global__ void __launch_bounds__(256) sf_expand_kernel(DispatchParams p) {
+  const int nb = p.H / kFp8Block;
+  const int64_t total = min((int64_t)__ldg(p.num_rows), p.rows_alloc);
+  const int2 *meta = reinterpret_cast<const int2 *>(p.meta);
+  for (int64_t row = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; row < total;
+       row += (int64_t)gridDim.x * blockDim.x) {
+    const int tok = __ldg(&meta[row].x);
+    const float *src = p.tok_scale + (int64_t)(tok >= 0 ? tok : 0) * nb;
+    float *dst = p.recv_sf + row;
+    int j = 0;
+    if ((nb & 3) == 0) {
+      for (; j < nb; j += 4) {
+        float4 v = tok >= 0 ? __ldg(reinterpret_cast<const float4 *>(src + j)) : make_float4(0, 0, 0, 0);
+        dst[(int64_t)j * p.sf_hidden_stride] = v.x;
+        dst[(int64_t)(j + 1) * p.sf_hidden_stride] = v.y;
+        dst[(int64_t)(j + 2) * p.sf_hidden_stride] = v.z;
+        dst[(int64_t)(j + 3) * p.sf_hidden_stride] = v.w;
+      }
+    }
+    for (; j < nb; ++j) dst[(int64_t)j * p.sf_hidden_stride] = tok >= 0 ? __ldg(src + j) : 0.f;
+  }
+}
+
+template <bool FP8, bool CM>
+cudaError_t launch_one(const DispatchParams &p, int sm_cap, cudaStream_t s) {
+  auto kern = dispatch_kernel<FP8, CM>;
+  const int H = p.H;
+  const int nvec = H / 8;
+  // FP8: consumer threads cover the row in whole 16-lane groups; BF16: the
+  // consumers only issue bulk copies and zero padding rows.
+  const int consumers = FP8 ? std::min(kMaxConsumers, (nvec + 31) / 32 * 32) : 64;
+  const int threads = consumers + 32;
+  const size_t in_stage = (size_t)(2 * H + 127) / 128 * 128;
+  const size_t out_stage = FP8 ? (size_t)(H + 127) / 128 * 128 : 0;
+  const size_t smem = kStages * (in_stage + out_stage) +
+                      (FP8 && !CM ? kStages * sizeof(float) * ((H / kFp8Block + 31) / 32 * 32) : 0);
+  cudaError_t err;
+  if (smem > 48 * 1024) {
+    err = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    if (err != cudaSuccess) return err;
+  }
+  int dev = 0;
+  err = cudaGetDevice(&dev);
+  if (err != cudaSuccess) return err;
+  int per_sm = 0;
+  err = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kern, threads, smem);
+  if (err != cudaSuccess) return err;
+  if (per_sm < 1) per_sm = 1;
+  const int sms = device_sm_count(dev);
+  const int use_sms = (sm_cap > 0 && sm_cap < sms) ? sm_cap : sms;
+  const int64_t items = (int64_t)p.T + p.max_pad_items;
+  const int64_t grid = std::min<int64_t>((int64_t)use_sms * per_sm, items);
+  if (grid <= 0) return cudaSuccess;
+  kern<<<(int)grid, threads, smem, s>>>(p);
+  err = cudaGetLastError();
+  if (err != cudaSuccess || !FP8 || !CM) return err;
+  // column-major scales: one gather pass (rows past the real total, in an
+  // upper-bound allocation, are left untouched)
+  const int64_t sf_grid = std::min<int64_t>((p.rows_alloc + 255) / 256, (int64_t)use_sms * 8);
+  if (sf_grid > 0) {
+    sf_expand_kernel<<<(int)sf_grid, 256, 0, s>>>(p);
+    err = cudaGetLastError();
+  }
+  return err;
+}
+
+}  // namespace
+
+cudaError_t launch_dispatch(const DispatchParams &p, int use_fp8, int col_major, int sm_cap,
+                            cudaStream_t s) {
+  if (use_fp8)
+    return col_major ? launch_one<true, true>(p, sm_cap, s) : launch_one<true, false>(p, sm_cap, s);
+  return launch_one<false, false>(p, sm_cap, s);
+}
+
+}  // namespace ep

@@ -1,0 +1,100 @@
+// Internal declarations shared by the translation units of libep.so.
+#pragma once
+
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "../../include/ep.h"
+
+namespace ep {
+
+constexpr int kFp8Block = 128;          // 1x128 scale blocks
+constexpr int kLayoutThreads = 1024;     // assign kernel CTA
+constexpr int kLayoutChunkTokens = 256;  // tokens per layout chunk (<= 8192 slots with K <= 32)
+
+// Control words at the head of the handle's device block.
+enum CtrlSlot { kCtrlError = 0, kCtrlNumRecv = 2, kCtrlNumExpanded = 3, kCtrlWords = 8 };
+
+// Pinned, device-mapped host words the count wait polls (do_cpu_sync).
+struct HostSync {
+  volatile int32_t flag;
+  volatile int32_t error;
+  volatile int32_t num_recv;
+  volatile int32_t num_expanded;
+  int32_t pad[12];
+};
+
+// Everything a layout kernel needs; passed by value.
+struct LayoutParams {
+  const void *topk_idx;   // caller's [T, K]
+  int idx_is_int64;
+  int T, K, E, R, L, M, A;
+  int do_expand;
+  int num_blocks;         // layout grid (one CTA per chunk of tokens)
+  int blocks_per_src;     // chunks per source rank
+  int chunk_tokens;       // tokens per chunk
+  int rank_warps;         // warps that rank slots in the assign kernel
+  int64_t row_limit;      // rows at or past this are dropped (overflow)
+  int32_t *topk32;        // [T, K]
+  int32_t *dst;           // [T, K]
+  int32_t *meta;          // [row_limit, 2]
+  uint8_t *in_rank;       // [T, R]
+  int32_t *cnt_e, *cnt_e_al, *psum_e;   // [E], [E], [E+1]
+  int32_t *psum_pad;      // [E+1] exclusive prefix of the padding rows per expert
+  int32_t *cnt_r, *psum_r, *psum_rs;    // [R], [R+1], [R, R+1]
+  int32_t *ctrl;          // kCtrl* words
+  int32_t *blk_e;         // [num_blocks, E] per-chunk expert counts
+  int32_t *blk_r;         // [num_blocks, R] per-chunk rank counts
+  unsigned *blk_err;      // [num_blocks] per-chunk EP_ERRBIT_* bits
+  HostSync *host;         // device view of the mapped host words, or nullptr
+  int32_t seq;            // value the count wait looks for
+};
+
+struct DispatchParams {
+  const uint16_t *x;      // [T, H] bf16 bits
+  const float *topk_w;    // [T, K] or nullptr
+  const int32_t *topk32;  // [T, K]
+  const int32_t *dst;     // [T, K]
+  const int32_t *psum_e;  // [E+1]
+  const int32_t *cnt_e;   // [E]
+  const int32_t *psum_pad;  // [E+1] padding rows before expert e
+  int T, K, E, L, H;
+  int do_expand, zero_padding;
+  int64_t max_pad_items;  // upper bound on padding work items (grid sizing only)
+  int64_t rows_alloc;     // rows of recv_*
+  int64_t sf_hidden_stride, sf_token_stride;
+  void *recv_x;
+  float *recv_sf;
+  float *recv_w;
+  int32_t *recv_idx;
+  unsigned *err;          // the handle's error word (EP_ERRBIT_TIMEOUT)
+  float *tok_scale;       // [T, H/128] FP8 scales per source token (handle scratch)
+  const int32_t *meta;    // [rows, 2] recv_src_metadata
+  const int32_t *num_rows;  // device total rows of the layout
+};
+
+struct CombineParams {
+  const uint16_t *y;      // [rows_alloc, H]
+  const float *topk_w;    // [T, K] or nullptr
+  const int32_t *topk32;  // [T, K]
+  const int32_t *dst;     // [T, K]
+  const uint16_t *bias0, *bias1;  // [T, H] or nullptr
+  const uint16_t *ebias;  // [E, H] or nullptr
+  uint16_t *out;          // [T, H]
+  unsigned *err;          // the handle's error word (EP_ERRBIT_TIMEOUT)
+  int T, K, H;
+  int64_t rows_alloc;
+};
+
+// Launchers (return the first CUDA error, cudaSuccess otherwise).
+cudaError_t launch_layout(const LayoutParams &p, cudaStream_t s);
+size_t layout_assign_smem(const LayoutParams &p);
+int layout_rank_warps(int nkey);
+cudaError_t launch_dispatch(const DispatchParams &p, int use_fp8, int col_major,
+                            int sm_cap, cudaStream_t s);
+cudaError_t launch_combine(const CombineParams &p, int sm_cap, cudaStream_t s);
+
+// Device facts, cached per device.
+int device_sm_count(int device);
+
+}  // namespace ep

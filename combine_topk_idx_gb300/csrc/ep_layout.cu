@@ -1,0 +1,436 @@
+// Routing layout: counts, prefix sums, destination rows and source metadata.
+//
+// Follows the layout contract of "DeepEP V2 notes, ch. 7: how V2 dispatch
+// builds expert inputs" (§7.2 layout metadata, §7.4 expanded layout) and the
+// get_dispatch_layout outputs of the DeepEP README interface example.
+//
+// Tokens are cut into chunks of up to kLayoutChunkTokens tokens that never
+// straddle a source rank; one CTA owns one chunk in both kernels (256 threads,
+// one per token, in count; 1024 in assign).
+//   count  - one thread per token: validates and copies topk_idx, builds the
+//            token's rank set (is_token_in_rank, first slot per rank) and
+//            adds to the CTA's expert / rank histograms, stored block-major.
+//   assign - every CTA sums the histogram columns it needs (global totals
+//            and the totals of the chunks before it), scans them into segment
+//            starts, then ranks its own slots stably: warps walk contiguous
+//            runs of (token, slot) pairs in order, ranking equal keys with
+//            __match_any_sync.  Row = segment start + earlier chunks +
+//            earlier warps + earlier lanes, i.e. ascending (token, slot)
+//            inside every segment, with no atomics deciding positions.  CTA 0
+//            also writes the global counts and prefix sums (and, for the
+//            host count wait, the mapped totals).
+#include <algorithm>
+
+#include "ep_internal.cuh"
+
+namespace ep {
+namespace {
+
+constexpr int NT = kLayoutThreads;     // assign kernel: 1024 threads
+constexpr int NWARPS = NT / 32;
+constexpr int NTC = kLayoutChunkTokens;  // count kernel: one thread per token
+
+__device__ __forceinline__ int chunk_of(const LayoutParams &p, int b, int &t0) {
+  const int s = b / p.blocks_per_src;
+  const int c = b - s * p.blocks_per_src;
+  const int64_t start = (int64_t)s * p.M + (int64_t)c * p.chunk_tokens;
+  const int64_t src_end = min((int64_t)(s + 1) * p.M, (int64_t)p.T);
+  const int64_t end = min(start + p.chunk_tokens, src_end);
+  t0 = (int)min(start, (int64_t)p.T);
+  return end > start ? (int)(end - start) : 0;
+}
+
+// Exclusive scan of f(i), i < n, by the whole CTA into out[0..n]; returns the
+// total.  `warp_tot` is shared scratch of NWARPS + 1 ints.
+template <typename F>
+__device__ int cta_exclusive_scan(int n, F f, int32_t *out, int *warp_tot) {
+  const int per = (n + NT - 1) / NT;
+  const int beg = min(threadIdx.x * per, n);
+  const int end = min(beg + per, n);
+  int local = 0;
+  for (int i = beg; i < end; ++i) local += f(i);
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  int incl = local;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const int v = __shfl_up_sync(0xffffffffu, incl, o);
+    if (lane >= o) incl += v;
+  }
+  if (lane == 31) warp_tot[warp] = incl;
+  __syncthreads();
+  if (warp == 0) {
+    int w = lane < NWARPS ? warp_tot[lane] : 0;
+    int wi = w;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const int v = __shfl_up_sync(0xffffffffu, wi, o);
+      if (lane >= o) wi += v;
+    }
+    if (lane < NWARPS) warp_tot[lane] = wi - w;  // exclusive warp offsets
+    if (lane == NWARPS - 1) warp_tot[NWARPS] = wi;
+  }
+  __syncthreads();
+  int run = warp_tot[warp] + incl - local;
+  for (int i = beg; i < end; ++i) {
+    out[i] = run;
+    run += f(i);
+  }
+  const int total = warp_tot[NWARPS];
+  if (threadIdx.x == 0) out[n] = total;
+  __syncthreads();
+  return total;
+}
+
+__global__ void __launch_bounds__(NTC) layout_count_kernel(LayoutParams p) {
+  extern __shared__ __align__(16) int smem[];
+  const int K = p.K, L = p.L, R = p.R, E = p.E;
+  int *hist_e = smem;                       // [E]
+  int *hist_r = hist_e + E;                 // [R]
+  int *rank_of = hist_r + R;                // [E] owning rank of each expert
+  int *idx_s = rank_of + E;                 // [chunk_tokens * K]
+  __shared__ unsigned err_s;
+  const int b = blockIdx.x;
+  int t0;
+  const int nt = chunk_of(p, b, t0);
+  const int ns = nt * K;
+  const int64_t base = (int64_t)t0 * K;
+  const int lane = threadIdx.x & 31;
+  if (threadIdx.x == 0) err_s = 0;
+  for (int i = threadIdx.x; i < E + R; i += NTC) smem[i] = 0;
+  for (int e = threadIdx.x; e < E; e += NTC) rank_of[e] = e / L;
+
+  // Coalesced load of the chunk: validate and keep an int32 copy.
+  unsigned err = 0;
+  for (int i = threadIdx.x; i < ns; i += NTC) {
+    long long v = p.idx_is_int64 ? __ldg(static_cast<const long long *>(p.topk_idx) + base + i)
+                                 : __ldg(static_cast<const int *>(p.topk_idx) + base + i);
+    if (v < -1 || v >= E) {
+      err |= EP_ERRBIT_BAD_TOPK_IDX;
+      v = -1;
+    }
+    idx_s[i] = static_cast<int>(v);
+    p.topk32[base + i] = static_cast<int>(v);
+  }
+  err = __reduce_or_sync(0xffffffffu, err);
+  __syncthreads();
+  if (lane == 0 && err) atomicOr(&err_s, err);
+
+  // One thread per token: expert histogram and the token's rank set.
+  const int tl = threadIdx.x;
+  const bool active = tl < nt;
+  const int *trow = idx_s + tl * K;
+  uint64_t mask = 0;  // rank set (R <= 64)
+  if (active) {
+    for (int k = 0; k < K; ++k) {
+      const int e = trow[k];
+      if (e < 0) continue;
+      atomicAdd(&hist_e[e], 1);
+      const int r = rank_of[e];
+      if (R <= 64) {
+        mask |= 1ull << r;
+      } else {
+        bool first = true;  // wide rank sets: look back at this token's slots
+        for (int j = 0; j < k && first; ++j) first = !(trow[j] >= 0 && rank_of[trow[j]] == r);
+        if (first) atomicAdd(&hist_r[r], 1);
+      }
+    }
+  }
+  if (R <= 32) {
+    for (int r = 0; r < R; ++r) {
+      const int c = __popc(__ballot_sync(0xffffffffu, (mask >> r) & 1));
+      if (lane == 0 && c) atomicAdd(&hist_r[r], c);
+    }
+  } else if (R <= 64) {
+    for (uint64_t m = mask; m; m &= m - 1) atomicAdd(&hist_r[__ffsll((long long)m) - 1], 1);
+  }
+  if (active) {
+    uint8_t *row = p.in_rank + ((int64_t)t0 + tl) * R;
+    if (R <= 64) {
+      if ((R & 3) == 0) {
+        for (int r = 0; r < R; r += 4) {
+          const uint32_t w = (uint32_t)((mask >> r) & 1) | (uint32_t)((mask >> (r + 1)) & 1) << 8 |
+                             (uint32_t)((mask >> (r + 2)) & 1) << 16 |
+                             (uint32_t)((mask >> (r + 3)) & 1) << 24;
+          *reinterpret_cast<uint32_t *>(row + r) = w;
+        }
+      } else {
+        for (int r = 0; r < R; ++r) row[r] = (uint8_t)((mask >> r) & 1);
+      }
+    } else {
+      for (int r = 0; r < R; ++r) row[r] = 0;
+      for (int k = 0; k < K; ++k)
+        if (trow[k] >= 0) row[rank_of[trow[k]]] = 1;
+    }
+  }
+  __syncthreads();
+  for (int e = threadIdx.x; e < E; e += NTC) p.blk_e[(int64_t)b * E + e] = hist_e[e];
+  for (int r = threadIdx.x; r < R; r += NTC) p.blk_r[(int64_t)b * R + r] = hist_r[r];
+  if (threadIdx.x == 0) p.blk_err[b] = err_s;
+}
+
+__global__ void __launch_bounds__(NT) layout_assign_kernel(LayoutParams p) {
+  extern __shared__ __align__(16) int smem[];
+  const int K = p.K, L = p.L, E = p.E, R = p.R, A = p.A;
+  const int nkey = p.do_expand ? E : R;
+  const int cap = p.chunk_tokens * K;
+  int *idx_s = smem;                  // [cap]
+  int *row_s = idx_s + cap;           // [cap] sort key, then row
+  int *tot_s = row_s + cap;           // [E + R] global totals
+  int *bef_s = tot_s + E + R;         // [E + R] totals of the chunks before this one
+  int *seg_s = bef_s + E + R;         // [nkey + 1] segment starts
+  int *rank_of = seg_s + nkey + 1;    // [E] owning rank of each expert
+  // [rank_warps][nkey] 64-bit words: low half = running count of the key in
+  // the warp's range, high half = lanes holding the key in the current step
+  unsigned long long *whist =
+      reinterpret_cast<unsigned long long *>(rank_of + E + ((E + nkey + 1) & 1));
+  __shared__ int warp_tot[NWARPS + 1];
+
+  const int b = blockIdx.x;
+  int t0;
+  const int nt = chunk_of(p, b, t0);
+  const int ns = nt * K;
+  const int64_t base = (int64_t)t0 * K;
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  const int nrw = p.rank_warps;
+
+  for (int i = threadIdx.x; i < ns; i += NT) idx_s[i] = p.topk32[base + i];
+  for (int i = threadIdx.x; i < nrw * nkey; i += NT) whist[i] = 0ull;
+  for (int e = threadIdx.x; e < E; e += NT) rank_of[e] = e / L;
+  // Column sums of the per-chunk histograms: global totals and this chunk's offset.
+  for (int key = threadIdx.x; key < E + R; key += NT) {
+    const int32_t *col = key < E ? p.blk_e + key : p.blk_r + (key - E);
+    const int stride = key < E ? E : R;
+    int tot = 0, bef = 0;
+    int bb = 0;
+    for (; bb + 16 <= p.num_blocks; bb += 16) {
+      int v[16];
+#pragma unroll
+      for (int u = 0; u < 16; ++u) v[u] = __ldcg(col + (int64_t)(bb + u) * stride);
+#pragma unroll
+      for (int u = 0; u < 16; ++u) {
+        tot += v[u];
+        bef += (bb + u < b) ? v[u] : 0;
+      }
+    }
+    for (; bb < p.num_blocks; ++bb) {
+      const int v = __ldcg(col + (int64_t)bb * stride);
+      tot += v;
+      bef += (bb < b) ? v : 0;
+    }
+    tot_s[key] = tot;
+    bef_s[key] = bef;
+  }
+  __syncthreads();
+
+  // Segment starts of the sort key (aligned expert counts, or rank counts).
+  if (p.do_expand)
+    cta_exclusive_scan(E, [&](int e) { return (tot_s[e] + A - 1) / A * A; }, seg_s, warp_tot);
+  else
+    cta_exclusive_scan(R, [&](int r) { return tot_s[E + r]; }, seg_s, warp_tot);
+
+  if (b == 0) {
+    // Global outputs (written once, by CTA 0).  The sort key's prefix sum is
+    // seg_s already; the other one and the padding prefix take one scan each.
+    for (int e = threadIdx.x; e < E; e += NT) {
+      p.cnt_e[e] = tot_s[e];
+      p.cnt_e_al[e] = (tot_s[e] + A - 1) / A * A;
+    }
+    for (int r = threadIdx.x; r < R; r += NT) p.cnt_r[r] = tot_s[E + r];
+    int num_expanded, num_recv;
+    if (p.do_expand) {
+      for (int e = threadIdx.x; e <= E; e += NT) p.psum_e[e] = seg_s[e];
+      num_expanded = seg_s[E];
+      num_recv = cta_exclusive_scan(R, [&](int r) { return tot_s[E + r]; }, p.psum_r, warp_tot);
+    } else {
+      for (int r = threadIdx.x; r <= R; r += NT) p.psum_r[r] = seg_s[r];
+      num_recv = seg_s[R];
+      num_expanded = cta_exclusive_scan(E, [&](int e) { return (tot_s[e] + A - 1) / A * A; },
+                                        p.psum_e, warp_tot);
+    }
+    cta_exclusive_scan(E, [&](int e) { return (tot_s[e] + A - 1) / A * A - tot_s[e]; }, p.psum_pad,
+                       warp_tot);
+    unsigned err = 0;
+    for (int bb = threadIdx.x; bb < p.num_blocks; bb += NT) err |= __ldcg(p.blk_err + bb);
+    err = __reduce_or_sync(0xffffffffu, err);
+    if (lane == 0) warp_tot[warp] = static_cast<int>(err);
+    __syncthreads();
+    if (threadIdx.x == 0) {
+      for (int w = 1; w < NWARPS; ++w) err |= static_cast<unsigned>(warp_tot[w]);
+      const int64_t total_rows = p.do_expand ? num_expanded : num_recv;
+      if (total_rows > p.row_limit) err |= EP_ERRBIT_OVERFLOW;
+      p.ctrl[kCtrlError] = static_cast<int>(err);
+      p.ctrl[kCtrlNumRecv] = num_recv;
+      p.ctrl[kCtrlNumExpanded] = num_expanded;
+      if (p.host != nullptr) {
+        p.host->error = static_cast<int>(err);
+        p.host->num_recv = num_recv;
+        p.host->num_expanded = num_expanded;
+        __threadfence_system();
+        p.host->flag = p.seq;
+      }
+    }
+    // psum_rank_src[r][s]: tokens of source ranks < s received by rank r.
+    // Chunks are ordered by source rank; one warp scans each r over s.
+    const int src_ranks = p.num_blocks / p.blocks_per_src;
+    const int RR = R + 1;
+    for (int r = warp; r < R; r += NWARPS) {
+      int carry = 0;
+      if (lane == 0) p.psum_rs[(int64_t)r * RR] = 0;
+      for (int s0 = 0; s0 < R; s0 += 32) {
+        const int s = s0 + lane;
+        int c = 0;
+        if (s < R && s < src_ranks && p.T > 0) {
+          const int lo = s * p.blocks_per_src;
+          const int hi = min(lo + p.blocks_per_src, p.num_blocks);
+          for (int bb = lo; bb < hi; ++bb) c += __ldcg(p.blk_r + (int64_t)bb * R + r);
+        }
+        int incl = c;
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+          const int v = __shfl_up_sync(0xffffffffu, incl, o);
+          if (lane >= o) incl += v;
+        }
+        if (s < R) p.psum_rs[(int64_t)r * RR + s + 1] = carry + incl;
+        carry += __shfl_sync(0xffffffffu, incl, 31);
+      }
+    }
+  }
+
+  // Sort key per slot: the expert (expanded) or, for the lowest slot of the
+  // token on each rank, the rank (rank layout).
+  for (int i = threadIdx.x; i < ns; i += NT) {
+    const int e = idx_s[i];
+    int key = -1;
+    if (e >= 0) {
+      if (p.do_expand) {
+        key = e;
+      } else {
+        const int tl = i / K, k = i - tl * K;
+        const int r = rank_of[e];
+        bool first = true;
+        for (int j = 0; j < k && first; ++j) {
+          const int f = idx_s[tl * K + j];
+          first = !(f >= 0 && rank_of[f] == r);
+        }
+        if (first) key = r;
+      }
+    }
+    row_s[i] = key;
+  }
+  __syncthreads();
+
+  // Stable ranking: rank warp w owns the contiguous slot range [beg, end).
+  // Pass 1 counts keys per warp (shared-memory atomics, order-free); after
+  // the bases are known, pass 2 walks the range in order, 32 slots a step:
+  // every lane ORs its bit into its key's word, the word then names the
+  // lanes sharing the key (their order = slot order), and the lowest of them
+  // advances the key's running count.
+  const int per_warp = (ns + nrw - 1) / nrw;
+  const int beg = min(warp * per_warp, ns);
+  const int end = warp < nrw ? min(beg + per_warp, ns) : beg;
+  unsigned long long *wh = whist + (size_t)warp * nkey;
+  for (int i = beg + lane; i < end; i += 32) {
+    const int key = row_s[i];
+    if (key >= 0) atomicAdd(&wh[key], 1ull);
+  }
+  __syncthreads();
+  const int boff = p.do_expand ? 0 : E;
+  for (int key = threadIdx.x; key < nkey; key += NT) {
+    unsigned run = (unsigned)(seg_s[key] + bef_s[boff + key]);
+    for (int w = 0; w < nrw; ++w) {
+      const unsigned c = (unsigned)whist[(size_t)w * nkey + key];
+      whist[(size_t)w * nkey + key] = run;
+      run += c;
+    }
+  }
+  __syncthreads();
+  const unsigned lt = (1u << lane) - 1u;
+  for (int s0 = beg; s0 < end; s0 += 32) {
+    const int i = s0 + lane;
+    const int key = i < end ? row_s[i] : -1;
+    if (key >= 0) atomicOr(&wh[key], 1ull << (32 + lane));
+    __syncwarp();
+    const unsigned long long word = key >= 0 ? wh[key] : 0ull;
+    const unsigned peers = (unsigned)(word >> 32);
+    int row = -1;
+    if (key >= 0) row = (int)((unsigned)word + __popc(peers & lt));
+    __syncwarp();
+    if (key >= 0 && lane == __ffs(peers) - 1)
+      wh[key] = (unsigned long long)((unsigned)word + __popc(peers));
+    __syncwarp();
+    if (i < end) row_s[i] = row;
+  }
+  __syncthreads();
+
+  int2 *meta = reinterpret_cast<int2 *>(p.meta);
+  for (int i = threadIdx.x; i < ns; i += NT) {
+    const int tl = i / K, k = i - tl * K;
+    const int own = row_s[i];
+    int row = own;
+    const int e = idx_s[i];
+    if (!p.do_expand && e >= 0 && own < 0) {
+      // another (lower) slot of this token on the same rank owns the row
+      const int r = rank_of[e];
+      for (int j = 0; j < k; ++j) {
+        const int f = idx_s[tl * K + j];
+        if (f >= 0 && rank_of[f] == r) {
+          row = row_s[tl * K + j];
+          break;
+        }
+      }
+    }
+    if (row >= p.row_limit) row = -1;
+    p.dst[base + i] = row;
+    if (own >= 0 && own < p.row_limit) meta[own] = make_int2(t0 + tl, k);
+  }
+
+  if (p.do_expand) {
+    // alignment padding rows -> (-1, -1): one warp per expert, experts
+    // b + (warp + NWARPS * i) * gridDim.x
+    for (int e = b + warp * (int)gridDim.x; e < E; e += NWARPS * (int)gridDim.x) {
+      const int64_t r0 = (int64_t)seg_s[e] + tot_s[e];
+      const int64_t r1 = min((int64_t)seg_s[e + 1], p.row_limit);
+      for (int64_t r = r0 + lane; r < r1; r += 32) meta[r] = make_int2(-1, -1);
+    }
+  }
+}
+
+}  // namespace
+
+size_t layout_assign_smem(const LayoutParams &p) {
+  const int nkey = p.do_expand ? p.E : p.R;
+  return sizeof(int) * (2 * (size_t)p.chunk_tokens * p.K + 2 * (size_t)(p.E + p.R) + nkey + 1 +
+                        p.E + 1) +
+         sizeof(unsigned long long) * (size_t)p.rank_warps * nkey;
+}
+
+int layout_rank_warps(int nkey) {
+  // every warp ranks (a chunk has at most 8192 slots: 256 per warp); the
+  // per-warp key histograms stay within ~48 KB of shared memory
+  int w = NWARPS;
+  while (w > 1 && (size_t)w * nkey * sizeof(unsigned long long) > 64 * 1024) w >>= 1;
+  return w;
+}
+
+cudaError_t launch_layout(const LayoutParams &p, cudaStream_t s) {
+  const size_t smem_count = sizeof(int) * (2 * (size_t)p.E + p.R + (size_t)p.chunk_tokens * p.K);
+  const size_t smem_assign = layout_assign_smem(p);
+  cudaError_t err;
+  if (smem_count > 48 * 1024) {
+    err = cudaFuncSetAttribute(layout_count_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                               (int)smem_count);
+    if (err != cudaSuccess) return err;
+  }
+  if (smem_assign > 48 * 1024) {
+    err = cudaFuncSetAttribute(layout_assign_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                               (int)smem_assign);
+    if (err != cudaSuccess) return err;
+  }
+  layout_count_kernel<<<p.num_blocks, NTC, smem_count, s>>>(p);
+  err = cudaGetLastError();
+  if (err != cudaSuccess) return err;
+  layout_assign_kernel<<<p.num_blocks, NT, smem_assign, s>>>(p);
+  return cudaGetLastError();
+}
+
+}  // namespace ep

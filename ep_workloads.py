@@ -168,3 +168,26 @@ def make_inputs(name_or_wl, seed: int = 0, num_tokens: Optional[int] = None) -> 
 
 def replace(wl: Workload, **kw) -> Workload:
     return dataclasses.replace(wl, **kw)
+
+
+def hashed_bf16_rows(rows, hidden: int, seed: int, device="cpu") -> torch.Tensor:
+    """Counter-based BF16 matrix: element (r, c) depends only on (seed, r, c).
+
+    Rows can be produced one subset at a time and on any device with
+    identical bits, so the CPU side can rebuild exactly the rows it needs of
+    a large matrix that lives in device memory.  Integer arithmetic only
+    (every product stays below 2^62, so nothing overflows int64).  Values
+    are +-m * 2^k with k in [-3, 1], roughly unit scale.
+    """
+    r = torch.as_tensor(rows, dtype=torch.int64, device=device).reshape(-1, 1)
+    c = torch.arange(hidden, dtype=torch.int64, device=device).reshape(1, -1)
+    m31 = 0x7FFFFFFF
+    h = (r * 40503 + c * 2654435 + seed * 97 + 12345) & m31
+    for _ in range(3):
+        h = ((h * 1103515245 + 12345) & m31) ^ (h >> 13)
+    sign = (h & 1) << 15
+    expo = 124 + ((h >> 1) % 5)                # biased exponent 124..128
+    mant = (h >> 4) & 0x7F
+    bits = sign | (expo << 7) | mant
+    bits = torch.where(bits >= 0x8000, bits - 0x10000, bits).to(torch.int16)
+    return bits.view(torch.bfloat16)

@@ -1,0 +1,239 @@
+/*
+ * ep.h -- C ABI of the single-GPU MoE dispatch / combine library (libep.so).
+ *
+ * One GPU, logical ranks: the experts 0..E-1 are owned by R logical ranks in
+ * contiguous blocks of L = E / R; token t comes from logical rank t / M
+ * (M = num_max_tokens_per_rank).  The three steps of the hot path are
+ *
+ *   ep_layout    routing layout from topk_idx: counts, prefix sums, the
+ *                destination row of every (token, slot) and per-row source
+ *                metadata;
+ *   ep_dispatch  copy epilogue: the rows of x (BF16, or FP8 e4m3 with 1x128
+ *                fp32 scales) land in the rank layout or in the expert-
+ *                expanded, alignment-padded layout;
+ *   ep_combine   per-token weighted gather-reduce of the expert outputs back
+ *                to source-token order, fp32 accumulation, BF16 result;
+ *
+ * plus ep_handle_free.  The arguments follow the dispatch / combine / handle
+ * contract described in "DeepEP V2 notes, ch. 7: how V2 dispatch builds
+ * expert inputs" (§7.1 input contract, §7.2 layout metadata and allocation,
+ * §7.3 copy epilogue, §7.5 handle reuse) and "DeepEP V2 notes, ch. 8:
+ * combine, handle and async overlap" (§8.1 combine along the handle, §8.2
+ * streams).  There is no communication: every "rank" lives in this GPU's HBM.
+ *
+ * Conventions for every entry point
+ *   - All pointers named x, y, recv_*, out, bias*, topk_* are DEVICE pointers
+ *     owned by the caller; `cfg`, `info`, `out_handle`, `rows` are HOST
+ *     pointers.  Matrices are dense row-major with no padding between rows.
+ *   - All work is enqueued on `stream` (a cudaStream_t; NULL = legacy default
+ *     stream) and is ordered after earlier work on that stream.  Nothing is
+ *     synchronised with the host except the count wait of do_cpu_sync.
+ *   - Errors are returned as ep_status; no exception crosses the ABI.  On any
+ *     status other than EP_OK (and EP_ERR_BAD_TOPK_IDX, see ep_layout)
+ *     nothing is allocated and no output is defined.
+ *   - The calling thread's current CUDA device must be the device that owns
+ *     the pointers.
+ */
+#ifndef EP_H_
+#define EP_H_
+
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+#if defined(__GNUC__)
+#define EP_API __attribute__((visibility("default")))
+#else
+#define EP_API
+#endif
+
+/* Same type as cudaStream_t (struct CUstream_st *). */
+typedef struct CUstream_st *ep_stream_t;
+
+typedef enum ep_status {
+  EP_OK = 0,
+  EP_ERR_INVALID_ARG = 1,   /* bad config value, NULL or misaligned pointer */
+  EP_ERR_UNSUPPORTED = 2,   /* valid but outside this build's limits */
+  EP_ERR_BAD_TOPK_IDX = 3,  /* a topk_idx value outside [-1, num_experts) */
+  EP_ERR_CUDA = 4,          /* a CUDA runtime call failed */
+  EP_ERR_OOM = 5,           /* device or pinned host allocation failed */
+  EP_ERR_TIMEOUT = 6,       /* do_cpu_sync: counts not ready before the deadline */
+  EP_ERR_OVERFLOW = 7       /* upper-bound allocation exceeded (repeated experts) */
+} ep_status;
+
+/* Bits of the device error word (ep_layout_info.error_word). */
+#define EP_ERRBIT_BAD_TOPK_IDX 1u  /* value outside [-1, E): the slot is treated as empty */
+#define EP_ERRBIT_OVERFLOW 2u      /* rows at or past rows_alloc were dropped */
+#define EP_ERRBIT_TIMEOUT 4u       /* a bounded device-side wait gave up (output undefined) */
+
+/* Build limits (checked by ep_validate_config). */
+#define EP_MAX_TOPK 32
+#define EP_MAX_EXPERTS 2048
+#define EP_MAX_HIDDEN 32768
+
+/*
+ * Parameters of one layout; copied into the handle.  Field meaning follows
+ * the dispatch arguments of §7.2 (num_experts, expert_alignment,
+ * num_max_tokens_per_rank, do_cpu_sync, do_expand, do_zero_padding,
+ * use_tma_aligned_col_major_sf) and §7.1 (topk).
+ */
+typedef struct ep_config {
+  int32_t num_tokens;               /* T >= 0 */
+  int32_t num_topk;                 /* K in [1, EP_MAX_TOPK] */
+  int32_t num_experts;              /* E in [1, EP_MAX_EXPERTS], E % R == 0 */
+  int32_t num_ranks;                /* R >= 1 logical ranks */
+  int32_t hidden;                   /* H, multiple of 8 (of 128 with use_fp8) */
+  int32_t num_max_tokens_per_rank;  /* M >= 1, T <= M * R */
+  int32_t expert_alignment;         /* A >= 1 */
+  int32_t topk_idx_is_int64;        /* 1: topk_idx is int64 (torch default), 0: int32 */
+  uint8_t do_expand;                /* 1: expert-expanded layout, 0: rank layout */
+  uint8_t do_zero_padding;          /* expanded only: zero the alignment padding rows */
+  uint8_t do_cpu_sync;              /* 1: wait for the counts, exact allocation */
+  uint8_t use_fp8;                  /* dispatch quantises to e4m3 + fp32 scales */
+  uint8_t use_tma_aligned_col_major_sf; /* FP8 scales column-major, 16 B aligned */
+  uint8_t reserved0[3];             /* must be 0 */
+  int32_t num_sms;                  /* 0 = all SMs; otherwise cap on the SMs used */
+  int32_t cpu_sync_timeout_ms;      /* do_cpu_sync deadline; 0 = 10000 ms */
+} ep_config;
+
+/*
+ * Filled by ep_layout.  Device pointers are owned by the handle and stay
+ * valid until ep_handle_free; they are stream-ordered on the layout stream.
+ */
+typedef struct ep_layout_info {
+  int64_t num_recv_tokens;      /* rank-layout rows; exact with do_cpu_sync, else -1 */
+  int64_t num_expanded_tokens;  /* aligned expanded rows; exact with do_cpu_sync, else -1 */
+  int64_t rows_alloc;           /* rows the caller allocates for recv_x and friends:
+                                   the exact total (do_cpu_sync) or the upper bound */
+  int64_t sf_numel;             /* fp32 elements of recv_sf (FP8 only, else 0) */
+  int64_t sf_token_stride;      /* recv_sf[row * sf_token_stride + j * sf_hidden_stride] */
+  int64_t sf_hidden_stride;
+  const int32_t *topk_idx;            /* [T, K] int32 copy, invalid values -> -1 */
+  const int32_t *cnt_expert;          /* [E] valid slots per expert (unaligned) */
+  const int32_t *cnt_expert_aligned;  /* [E] counts rounded up to A */
+  const int32_t *psum_expert;         /* [E+1] exclusive prefix of the aligned counts */
+  const int32_t *cnt_rank;            /* [R] tokens received per rank */
+  const int32_t *psum_rank;           /* [R+1] exclusive prefix of cnt_rank */
+  const int32_t *psum_rank_src;       /* [R, R+1] per receiving rank, prefix over source ranks */
+  const int32_t *dst_buffer_slot_idx; /* [T, K] destination row or -1 */
+  const int32_t *recv_src_metadata;   /* [rows, 2] (token, slot) per row, (-1,-1) padding */
+  const uint8_t *is_token_in_rank;    /* [T, R] 0/1 */
+  const int32_t *totals;              /* [2] device num_recv_tokens, num_expanded_tokens */
+  const uint32_t *error_word;         /* [1] EP_ERRBIT_* bits */
+  int64_t meta_rows;                  /* rows of recv_src_metadata */
+} ep_layout_info;
+
+typedef struct ep_handle ep_handle;
+
+/*
+ * ep_layout -- routing layout (DeepEP README interface example,
+ * get_dispatch_layout; §7.2 layout metadata; §7.4 expanded layout).
+ *
+ * topk_idx: device [T, K], int64 or int32 per cfg->topk_idx_is_int64; -1 is
+ *   an empty slot.  It is read only during this call (the handle keeps an
+ *   int32 copy), so the caller may reuse it once the stream passes the call.
+ * Rows: expert e's segment starts at psum_expert[e] (expanded) or rank r's at
+ *   psum_rank[r] (rank layout); inside a segment rows follow ascending
+ *   (token, slot).  In the rank layout all slots of a token on one rank share
+ *   one row.
+ * do_cpu_sync = 1: blocks the host until the counts are visible (polling
+ *   mapped host memory, deadline cfg->cpu_sync_timeout_ms), then reports the
+ *   exact totals; not allowed while `stream` is being captured.  Returns
+ *   EP_ERR_TIMEOUT at the deadline (no handle), EP_ERR_BAD_TOPK_IDX if a
+ *   value was outside [-1, E) -- the handle is still created, with those
+ *   slots empty, and must be freed.
+ * do_cpu_sync = 0: no host synchronisation (graph-capturable); rows_alloc is
+ *   the upper bound and the device totals / error word tell the real sizes.
+ * On EP_OK (or EP_ERR_BAD_TOPK_IDX) *out_handle owns device memory allocated
+ *   stream-ordered on `stream`; release it with ep_handle_free.
+ */
+EP_API ep_status ep_layout(const ep_config *cfg, const void *topk_idx, ep_stream_t stream,
+                    ep_handle **out_handle, ep_layout_info *info);
+
+/*
+ * ep_dispatch -- copy epilogue (§7.3 launch_dispatch_copy_epilogue, §7.4).
+ *
+ * x: device BF16 [T, H], 16-byte aligned.
+ * topk_weights: device fp32 [T, K] or NULL (then recv_topk_weights must be NULL).
+ * recv_x: [rows_alloc, H] BF16, or e4m3 bytes when cfg->use_fp8; 16-byte aligned.
+ * recv_sf: FP8 only, fp32 [sf_numel]; row-major [rows_alloc, H/128] or, with
+ *   use_tma_aligned_col_major_sf, column-major with hidden stride
+ *   align(rows_alloc, 4).  scale = amax / 448 per 1x128 block (fp32 IEEE
+ *   division), payload = e4m3(x / scale) round-to-nearest-even, saturating;
+ *   an all-zero block has scale 0 and zero bytes.
+ * recv_topk_weights: NULL, or fp32 [rows_alloc] (expanded) / [rows_alloc, K]
+ *   (rank layout: the token's weights on that rank, 0 elsewhere).
+ * recv_topk_idx: NULL, or (rank layout only) int32 [rows_alloc, K]: the local
+ *   expert index (expert - r * L) of the token's slots on that rank, -1 elsewhere.
+ * Padding rows (expanded) get weight 0; with do_zero_padding also zero
+ *   payload and zero scales.  Rows past the real total are not written.
+ * Must be ordered after ep_layout of the same handle (same stream, or the
+ *   caller's own event).  May be called again with new x (cached dispatch).
+ */
+EP_API ep_status ep_dispatch(ep_handle *h, const void *x, const float *topk_weights,
+                      void *recv_x, float *recv_sf, float *recv_topk_weights,
+                      int32_t *recv_topk_idx, ep_stream_t stream);
+
+/*
+ * ep_combine -- reduce expert outputs back to token order (§8.1 combine
+ * along the handle; vLLM PR #52781 review: combine requires BF16 input and
+ * may be called with topk_weights = None).
+ *
+ * y: device BF16 [rows_alloc, H] in the dispatch layout, 16-byte aligned.
+ * out: device BF16 [T, H], 16-byte aligned; must not overlap y.
+ * For each token: acc = 0 (fp32); for k = 0..K-1 over valid slots:
+ *   v = y[dst[t,k]] (+ expert_bias[topk_idx[t,k]] if given);
+ *   acc += topk_weights[t,k] * v (product and sum each rounded to fp32).
+ *   With topk_weights == NULL the weight is 1 and a row already used by an
+ *   earlier slot of the same token is skipped (rank layout shares rows).
+ *   Then acc += bias_0[t], acc += bias_1[t]; out[t] = bf16_rne(acc).
+ * bias_0, bias_1: NULL or device BF16 [T, H]; expert_bias: NULL or BF16 [E, H].
+ */
+EP_API ep_status ep_combine(const ep_handle *h, const void *y, const float *topk_weights,
+                     const void *bias_0, const void *bias_1, const void *expert_bias,
+                     void *out, ep_stream_t stream);
+
+/*
+ * ep_handle_free -- releases the handle's device memory, stream-ordered on
+ * the stream given to ep_layout (work enqueued there before this call may
+ * still use it).  NULL is ignored.  Work on other streams that uses the
+ * handle must be ordered before this call by the caller.
+ */
+EP_API void ep_handle_free(ep_handle *h);
+
+/* ---- host-only helpers (no GPU needed) ---------------------------------- */
+
+/* Human-readable name of a status code (static string). */
+EP_API const char *ep_status_string(ep_status s);
+
+/* ABI version of this header (bumped on any layout change of the structs). */
+EP_API int32_t ep_abi_version(void);
+
+/* Checks cfg against the rules above without touching the GPU. */
+EP_API ep_status ep_validate_config(const ep_config *cfg);
+
+/*
+ * Upper-bound rows for cfg (§7.2 worst case, ranks packed back to back):
+ * min(R * per_rank, global) with per_rank = M * R (rank layout) or
+ * align(R * M * min(K, L) + (A - 1) * L, A) (expanded) and global =
+ * T * min(K, R) or align(T * K + E * (A - 1), A).  Host only.
+ */
+EP_API ep_status ep_upper_bound_rows(const ep_config *cfg, int64_t *rows);
+
+/*
+ * The host wait used by do_cpu_sync: polls *flag until it equals `expected`
+ * or `timeout_ms` passes (EP_ERR_TIMEOUT).  Exposed so the deadline logic can
+ * be tested on the host with a flag that nothing sets.
+ */
+EP_API ep_status ep_host_wait_flag(const volatile int32_t *flag, int32_t expected,
+                            int32_t timeout_ms);
+
+#define EP_ABI_VERSION 1
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* EP_H_ */

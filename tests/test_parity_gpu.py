@@ -1,0 +1,323 @@
+"""GPU parity: the CUDA path (through the C ABI) against the CPU oracle.
+
+Layout, metadata and dispatch payload (BF16 bytes, FP8 bytes and scales) must
+match bit for bit; combine within 1 BF16 ulp per element (the kernel rounds
+every operation exactly like the oracle, so in practice it is bit-exact and
+the test also reports the number of differing elements).
+"""
+import zlib
+
+import numpy as np
+import pytest
+import torch
+
+import ep_workloads as W
+from oracle import ep_oracle as O
+from tests import ep_harness as HN
+
+pytestmark = pytest.mark.gpu
+
+COMBINE_ULP = 1  # tolerance stated for combine (1 BF16 ulp per element)
+
+
+@pytest.fixture(scope="module")
+def ep():
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    import combine_topk_idx_gb300 as ep
+    ep.load_library()
+    return ep
+
+
+def make_y(rows: int, H: int, seed: int, device) -> torch.Tensor:
+    out = torch.empty((rows, H), dtype=torch.bfloat16, device=device)
+    step = 8192
+    for r0 in range(0, rows, step):
+        r1 = min(rows, r0 + step)
+        out[r0:r1] = W.hashed_bf16_rows(torch.arange(r0, r1, device=device), H, seed, device)
+    return out
+
+
+def run_and_check(ep, cfg, idx_cpu, x_cpu, w_cpu, *, y_seed=11, combine_tokens=None,
+                  dispatch_tokens=None, with_weights=True, with_idx=True, combine_w=True,
+                  bias0=False, bias1=False, expert_bias=None):
+    dev = torch.device("cuda")
+    idx = idx_cpu.to(dev)
+    x = x_cpu.to(dev)
+    w = w_cpu.to(dev) if w_cpu is not None else None
+    h = ep.ep_layout(cfg, idx)
+    lay = HN.oracle_layout(cfg, idx_cpu.to(torch.int64).numpy())
+    HN.check_layout(h, lay)
+    use_fp8, cm = bool(cfg.use_fp8), bool(cfg.use_tma_aligned_col_major_sf)
+    out = ep.alloc_recv(h, with_weights=with_weights and w is not None,
+                        with_idx=with_idx and not cfg.do_expand)
+    ep.ep_dispatch(h, x, w, **out)
+    x_bits = HN.bits16(x_cpu)
+    w_np = None if w_cpu is None else w_cpu.numpy()
+    if dispatch_tokens is None:
+        d_or = O.dispatch(lay, x_bits, w_np, use_fp8, cm, bool(cfg.do_zero_padding))
+        HN.check_dispatch(h, lay, d_or, out, use_fp8, cm)
+    else:
+        d_or = HN.oracle_dispatch_tokens(x_bits, dispatch_tokens, use_fp8)
+        HN.check_dispatch(h, lay, d_or, out, use_fp8, cm, tokens=dispatch_tokens)
+        if cfg.do_expand and cfg.do_zero_padding:
+            HN.check_padding_zero(lay, out, use_fp8, cm)
+
+    # combine on a counter-based y so the oracle can rebuild any rows it needs
+    T, H = cfg.num_tokens, cfg.hidden
+    rows = h.rows_alloc
+    y = make_y(rows, H, y_seed, dev)
+    b0 = W.hashed_bf16_rows(torch.arange(T), H, y_seed + 1, dev) if bias0 else None
+    b1 = W.hashed_bf16_rows(torch.arange(T), H, y_seed + 2, dev) if bias1 else None
+    eb = expert_bias.to(dev) if expert_bias is not None else None
+    cw = w if combine_w else None
+    res = ep.ep_combine(h, y, cw, b0, b1, eb)
+    torch.cuda.synchronize()
+    toks = np.arange(T) if combine_tokens is None else np.asarray(combine_tokens)
+    need = np.unique(lay["dst_buffer_slot_idx"][toks])
+    need = need[need >= 0]
+    y_bits = np.zeros((max(rows, 1), H), dtype=np.uint16)
+    if need.size:
+        y_bits[need] = HN.bits16(W.hashed_bf16_rows(torch.from_numpy(need), H, y_seed))
+    ref = O.combine(lay, y_bits, None if cw is None else w_np,
+                    None if b0 is None else HN.bits16(b0.cpu()),
+                    None if b1 is None else HN.bits16(b1.cpu()),
+                    None if eb is None else HN.bits16(expert_bias), tokens=toks)
+    got = HN.bits16(res.index_select(0, torch.from_numpy(toks).to(dev)) if combine_tokens is not None
+                    else res)
+    d = HN.ulp_diff(got, ref)
+    assert d.max(initial=0) <= COMBINE_ULP, f"combine max ulp diff {d.max(initial=0)}"
+    h.free()
+    return {"lay": lay, "combine_mismatch": int((d != 0).sum())}
+
+
+# ---------------------------------------------------------------------------
+# The five workloads
+# ---------------------------------------------------------------------------
+@pytest.mark.parametrize("name", ["tiny", "decode", "prefill", "skewed"])
+def test_workload_parity(ep, name):
+    wl = W.WORKLOADS[name]
+    inp = W.make_inputs(wl, seed=0)
+    cfg = HN.cfg_for(ep, wl)
+    T = wl.num_tokens
+    big = T * wl.hidden > 4_000_000
+    rng = np.random.default_rng(1)
+    ct = np.sort(rng.choice(T, size=min(T, 384), replace=False)) if big else None
+    r = run_and_check(ep, cfg, inp["topk_idx"], inp["x"], inp["topk_weights"],
+                      combine_tokens=ct, bias0=(name == "tiny"), bias1=(name == "tiny"),
+                      expert_bias=inp["expert_bias"])
+    assert r["combine_mismatch"] == 0
+
+
+@pytest.mark.parametrize("name", ["tiny", "decode", "prefill", "skewed", "large"])
+def test_workload_parity_reduced_tokens(ep, name):
+    """Every workload's routing regime at a token count the oracle finishes fast,
+    spanning several layout CTAs and a ragged last chunk; full combine parity."""
+    wl = W.WORKLOADS[name]
+    T = min(wl.num_tokens, 700)
+    inp = W.make_inputs(wl, seed=5, num_tokens=T)
+    cfg = HN.cfg_for(ep, wl, T=T, M=max(37, -(-T // wl.num_ranks)))
+    run_and_check(ep, cfg, inp["topk_idx"], inp["x"], inp["topk_weights"],
+                  expert_bias=inp["expert_bias"])
+
+
+def test_large_full_size_sampled(ep):
+    wl = W.WORKLOADS["large"]
+    inp = W.make_inputs(wl, seed=0)
+    cfg = HN.cfg_for(ep, wl)
+    rng = np.random.default_rng(2)
+    toks = np.sort(rng.choice(wl.num_tokens, size=256, replace=False))
+    run_and_check(ep, cfg, inp["topk_idx"], inp["x"], inp["topk_weights"],
+                  combine_tokens=toks, dispatch_tokens=toks)
+
+
+# ---------------------------------------------------------------------------
+# Edge cases
+# ---------------------------------------------------------------------------
+def _routing(T, K, E, seed, drop=0.0, dup=False):
+    g = torch.Generator().manual_seed(seed)
+    if dup:
+        idx = torch.randint(0, E, (T, K), generator=g)
+    else:
+        idx = torch.rand(T, E, generator=g).topk(min(K, E), dim=1).indices
+        if K > E:
+            idx = torch.cat([idx, torch.full((T, K - E), -1, dtype=idx.dtype)], 1)
+    if drop > 0:
+        idx = idx.masked_fill(torch.rand(T, K, generator=g) < drop, -1)
+    w = torch.rand(T, K, generator=g).masked_fill(idx < 0, 0.0)
+    return idx.to(torch.int64).contiguous(), w.to(torch.float32).contiguous()
+
+
+EDGE = {
+    # name: (T, K, E, R, H, M, A, expand, zero_pad, sync, fp8, col_major, drop, dup)
+    "empty_tokens": (0, 4, 8, 2, 256, 4, 4, True, True, True, True, True, 0.0, False),
+    "empty_tokens_rank": (0, 4, 8, 2, 64, 4, 1, False, False, False, False, False, 0.0, False),
+    "all_slots_empty": (50, 3, 8, 4, 128, 13, 4, True, True, True, True, False, 1.0, False),
+    "all_empty_nosync": (50, 3, 8, 4, 64, 13, 4, True, True, False, False, False, 1.0, False),
+    "one_token": (1, 2, 4, 2, 128, 1, 8, True, True, True, True, True, 0.0, False),
+    "k1_r1": (300, 1, 5, 1, 72, 300, 1, True, False, True, False, False, 0.1, False),
+    "l1_rank_layout": (257, 6, 8, 8, 128, 33, 1, False, False, True, True, False, 0.2, False),
+    "ragged_bf16_h": (333, 4, 16, 4, 8 * 37, 100, 3, True, True, True, False, False, 0.1, False),
+    "ragged_fp8_h": (333, 4, 16, 4, 128 * 3, 100, 16, True, True, True, True, True, 0.1, False),
+    "fp8_rowmajor_expand": (200, 8, 32, 4, 512, 64, 32, True, True, True, True, False, 0.0, False),
+    "big_alignment": (90, 2, 8, 2, 128, 45, 256, True, True, True, True, True, 0.0, False),
+    "no_zero_padding": (128, 4, 16, 4, 256, 32, 8, True, False, True, True, True, 0.05, False),
+    "rank_nosync_fp8": (512, 8, 64, 8, 1024, 64, 1, False, False, False, True, False, 0.0, False),
+    "expand_nosync": (512, 8, 64, 8, 256, 64, 16, True, True, False, False, False, 0.0, False),
+    "dup_experts_sync_expand": (100, 6, 8, 2, 128, 50, 4, True, True, True, True, True, 0.1, True),
+    "dup_experts_rank": (100, 6, 8, 2, 128, 50, 1, False, False, True, False, False, 0.1, True),
+    "many_src_ranks_small_m": (1000, 4, 32, 32, 64, 32, 2, True, True, True, False, False, 0.0, False),
+    "max_topk": (64, 32, 64, 4, 128, 16, 4, True, True, True, True, True, 0.0, False),
+    "many_experts": (256, 8, 2048, 16, 128, 16, 4, True, True, True, True, True, 0.0, False),
+}
+
+
+@pytest.mark.parametrize("case", sorted(EDGE))
+def test_edge_cases(ep, case):
+    T, K, E, R, H, M, A, ex, zp, sync, fp8, cm, drop, dup = EDGE[case]
+    idx, w = _routing(T, K, E, seed=zlib.crc32(case.encode()) % 1000, drop=drop, dup=dup)
+    g = torch.Generator().manual_seed(3)
+    x = torch.randn(T, H, generator=g).to(torch.bfloat16)
+    cfg = ep.make_config(T, K, E, R, H, M, A, ex, zp, sync, fp8, cm)
+    run_and_check(ep, cfg, idx, x, w, bias0=True)
+
+
+def test_combine_variants(ep):
+    """No weights (rows used once), per-token biases, per-expert bias, both layouts."""
+    T, K, E, R, H, M = 300, 6, 16, 4, 256, 75
+    idx, w = _routing(T, K, E, seed=4, drop=0.1, dup=True)
+    x = torch.randn(T, H, generator=torch.Generator().manual_seed(5)).to(torch.bfloat16)
+    eb = W.hashed_bf16_rows(torch.arange(E), H, 99)
+    for expand in (False, True):
+        for combine_w in (True, False):
+            for b0, b1, e_b in [(False, False, None), (True, False, None), (False, True, eb),
+                                (True, True, eb)]:
+                run_and_check(ep, ep.make_config(T, K, E, R, H, M, 4 if expand else 1, expand,
+                                                 expand, True),
+                              idx, x, w, combine_w=combine_w, bias0=b0, bias1=b1, expert_bias=e_b)
+
+
+def test_int32_topk_idx(ep):
+    T, K, E, R, H, M = 400, 4, 32, 8, 128, 50
+    idx, w = _routing(T, K, E, seed=8, drop=0.1)
+    x = torch.randn(T, H).to(torch.bfloat16)
+    cfg = ep.make_config(T, K, E, R, H, M, 8, True, True, True, True, True)
+    run_and_check(ep, cfg, idx.to(torch.int32), x, w)
+
+
+def test_fp8_special_values(ep):
+    T, K, E, R, H = 16, 2, 4, 2, 512
+    idx = torch.tensor([[0, 3]] * T, dtype=torch.int64)
+    w = torch.full((T, K), 0.5)
+    xf = torch.randn(T, H, generator=torch.Generator().manual_seed(1))
+    xf[0, :128] = 0.0                    # zero block -> scale 0, zero bytes
+    xf[1, :] = -0.0                      # negative zeros
+    xf[2, :128] *= 1e-38                 # subnormal BF16 inputs, subnormal scale
+    xf[3, :] = 1.0                       # constant blocks
+    xf[4, :] = torch.tensor(np.random.default_rng(0).standard_cauchy(H), dtype=torch.float32)
+    xf[5, 5] = 3.0e38                    # near the BF16 maximum
+    xf[6, :] = torch.linspace(-448, 448, H)
+    xf[7, 0:128:2] = 1e-30
+    cfg = ep.make_config(T, K, E, R, H, 8, 4, True, True, True, True, True)
+    run_and_check(ep, cfg, idx, xf.to(torch.bfloat16), w)
+
+
+def test_bad_topk_idx_values(ep):
+    T, K, E, R, H, M = 40, 3, 8, 2, 128, 20
+    idx, w = _routing(T, K, E, seed=12)
+    idx[0, 1] = 8
+    idx[5, 0] = -7
+    idx[9, 2] = 1 << 40
+    x = torch.randn(T, H).to(torch.bfloat16)
+    for sync in (True, False):
+        cfg = ep.make_config(T, K, E, R, H, M, 4, True, True, sync, False)
+        h = ep.ep_layout(cfg, idx.cuda())
+        if sync:
+            assert h.status == ep.EP_ERR_BAD_TOPK_IDX
+        lay = HN.oracle_layout(cfg, idx.numpy())
+        assert lay["error"] == 1
+        HN.check_layout(h, lay)
+        h.free()
+        run_and_check(ep, cfg, idx, x, w)
+
+
+def test_overflow_with_repeated_experts(ep):
+    """No-sync expanded layout whose routing repeats experts beyond the printed
+    per-rank bound: rows past the allocation are dropped and flagged, and no
+    kernel writes past the caller's buffers (canary rows stay intact)."""
+    T, K, E, R, H, M = 2, 4, 2, 2, 128, 1
+    idx = torch.tensor([[0, 0, 0, 0], [1, 1, 0, 0]], dtype=torch.int64)
+    w = torch.full((T, K), 0.25)
+    x = torch.randn(T, H).to(torch.bfloat16)
+    cfg = ep.make_config(T, K, E, R, H, M, 1, True, True, False, True, True)
+    h = ep.ep_layout(cfg, idx.cuda())
+    lay = HN.oracle_layout(cfg, idx.numpy())
+    assert lay["error"] & 2 and h.rows_alloc == 4
+    HN.check_layout(h, lay)
+    canary = 5
+    big = torch.full((h.rows_alloc + canary, H), 0xA5, dtype=torch.uint8, device="cuda")
+    sf = torch.full((int(h.info.sf_numel) + 64,), -7.0, device="cuda")
+    rw = torch.full((h.rows_alloc + canary,), -3.0, device="cuda")
+    ep.ep_dispatch(h, x.cuda(), w.cuda(), big[:h.rows_alloc], sf[:int(h.info.sf_numel)],
+                   rw[:h.rows_alloc])
+    torch.cuda.synchronize()
+    assert int((big[h.rows_alloc:] != 0xA5).sum()) == 0
+    assert int((sf[int(h.info.sf_numel):] != -7.0).sum()) == 0
+    assert int((rw[h.rows_alloc:] != -3.0).sum()) == 0
+    h.free()
+    run_and_check(ep, cfg, idx, x, w)
+
+
+def test_output_canaries(ep):
+    """Dispatch and combine write nothing outside the rows they own."""
+    wl = W.WORKLOADS["tiny"]
+    inp = W.make_inputs(wl, seed=3)
+    cfg = HN.cfg_for(ep, wl)
+    h = ep.ep_layout(cfg, inp["topk_idx"].cuda())
+    rows, H, T = h.rows_alloc, wl.hidden, wl.num_tokens
+    pad = 7
+    rx = torch.full(((rows + pad) * H,), 0x5A5A, dtype=torch.int16, device="cuda").view(torch.bfloat16)
+    rw = torch.full((rows + pad,), 123.0, device="cuda")
+    ep.ep_dispatch(h, inp["x"].cuda(), inp["topk_weights"].cuda(),
+                   rx[:rows * H].view(rows, H), None, rw[:rows])
+    out = torch.full(((T + pad) * H,), 0x3C3C, dtype=torch.int16, device="cuda").view(torch.bfloat16)
+    y = make_y(rows, H, 3, "cuda")
+    ep.ep_combine(h, y, inp["topk_weights"].cuda(), out=out[:T * H].view(T, H))
+    torch.cuda.synchronize()
+    assert int((rx.view(torch.int16)[rows * H:] != 0x5A5A).sum()) == 0
+    assert int((rw[rows:] != 123.0).sum()) == 0
+    assert int((out.view(torch.int16)[T * H:] != 0x3C3C).sum()) == 0
+    h.free()
+
+
+def test_num_sms_cap_same_result(ep):
+    wl = W.WORKLOADS["prefill"]
+    inp = W.make_inputs(wl, seed=9, num_tokens=512)
+    for sms in (1, 3, 0):
+        cfg = HN.cfg_for(ep, wl, T=512, M=64, num_sms=sms)
+        run_and_check(ep, cfg, inp["topk_idx"], inp["x"], inp["topk_weights"])
+
+
+def test_layout_deterministic_and_cached_dispatch(ep):
+    """Two layouts of the same routing agree; one handle serves a second x."""
+    wl = W.WORKLOADS["skewed"]
+    T = 3000
+    inp = W.make_inputs(wl, seed=4, num_tokens=T)
+    cfg = HN.cfg_for(ep, wl, T=T, M=400)
+    idx = inp["topk_idx"].cuda()
+    h1, h2 = ep.ep_layout(cfg, idx), ep.ep_layout(cfg, idx)
+    a, b = HN.gpu_layout_arrays(h1), HN.gpu_layout_arrays(h2)
+    total = int(a["totals"][0])                 # rank layout: rows past it are unspecified
+    a["recv_src_metadata"] = a["recv_src_metadata"][:total]
+    b["recv_src_metadata"] = b["recv_src_metadata"][:total]
+    for k in a:
+        assert np.array_equal(a[k], b[k]), k
+    lay = HN.oracle_layout(cfg, inp["topk_idx"].numpy())
+    for seed in (1, 2):
+        x = W.make_x(wl, seed, num_tokens=T)
+        out = ep.alloc_recv(h1)
+        ep.ep_dispatch(h1, x.cuda(), None, **out)
+        d_or = O.dispatch(lay, HN.bits16(x), None, False, False, False)
+        HN.check_dispatch(h1, lay, d_or, out, False, False)
+    h1.free()
+    h2.free()

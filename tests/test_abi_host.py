@@ -1,0 +1,182 @@
+"""Host-only contract tests of the C ABI (no GPU needed, no compute call made).
+
+Modelled on the hermetic contract tests the vLLM PR #52781 review describes:
+they check argument validation, sizing, error codes and the host-side wait,
+never values computed on a device.  Every call here returns before the
+library touches the CUDA runtime.
+"""
+import ctypes
+import os
+import re
+import subprocess
+import tempfile
+import time
+
+import numpy as np
+import pytest
+
+from oracle import ep_oracle as O
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "ep.h")
+
+
+@pytest.fixture(scope="module")
+def ep():
+    import combine_topk_idx_gb300 as ep
+    from combine_topk_idx_gb300 import _build_lib
+    _build_lib.build()
+    ep.load_library()
+    return ep
+
+
+def _declared_symbols():
+    src = open(HEADER).read()
+    return sorted(set(re.findall(r"EP_API\s+[\w\s\*]+?\b(ep_\w+)\s*\(", src)))
+
+
+def test_library_exports_every_declared_symbol(ep):
+    names = _declared_symbols()
+    assert {"ep_layout", "ep_dispatch", "ep_combine", "ep_handle_free"} <= set(names)
+    lib = ep.load_library()
+    for n in names:
+        assert hasattr(lib, n), n
+    out = subprocess.run(["nm", "-D", "--defined-only", ep.LIB_PATH], capture_output=True,
+                         text=True, check=True).stdout
+    exported = set(re.findall(r"\bT (ep_\w+)", out))
+    assert set(names) <= exported
+    assert exported <= set(names), f"undeclared exports: {exported - set(names)}"
+    assert lib.ep_abi_version() == ep.EP_ABI_VERSION
+
+
+def test_struct_layout_matches_c_header(ep):
+    """ctypes mirrors of the ABI structs have the C compiler's sizes and offsets."""
+    prog = r'''
+#include <stddef.h>
+#include <stdio.h>
+#include "ep.h"
+#define P(T, f) printf(#T " " #f " %zu\n", offsetof(T, f));
+int main(void) {
+  printf("ep_config size %zu\n", sizeof(ep_config));
+  printf("ep_layout_info size %zu\n", sizeof(ep_layout_info));
+  P(ep_config, num_tokens) P(ep_config, topk_idx_is_int64) P(ep_config, do_expand)
+  P(ep_config, use_tma_aligned_col_major_sf) P(ep_config, num_sms) P(ep_config, cpu_sync_timeout_ms)
+  P(ep_layout_info, rows_alloc) P(ep_layout_info, topk_idx) P(ep_layout_info, error_word)
+  P(ep_layout_info, meta_rows)
+  return 0;
+}
+'''
+    with tempfile.TemporaryDirectory() as d:
+        c = os.path.join(d, "t.c")
+        open(c, "w").write(prog)
+        exe = os.path.join(d, "t")
+        subprocess.run(["gcc", "-std=c11", "-I", os.path.dirname(HEADER), c, "-o", exe], check=True)
+        lines = subprocess.run([exe], capture_output=True, text=True, check=True).stdout.split("\n")
+    got = {}
+    for ln in lines:
+        if ln:
+            a, b, v = ln.split()
+            got[(a, b)] = int(v)
+    C, I = ep.EpConfigC, ep.EpLayoutInfoC
+    assert got[("ep_config", "size")] == ctypes.sizeof(C)
+    assert got[("ep_layout_info", "size")] == ctypes.sizeof(I)
+    for f in ("num_tokens", "topk_idx_is_int64", "do_expand", "use_tma_aligned_col_major_sf",
+              "num_sms", "cpu_sync_timeout_ms"):
+        assert got[("ep_config", f)] == getattr(C, f).offset, f
+    for f in ("rows_alloc", "topk_idx", "error_word", "meta_rows"):
+        assert got[("ep_layout_info", f)] == getattr(I, f).offset, f
+
+
+def _cfg(ep, **kw):
+    base = dict(num_tokens=128, num_topk=2, num_experts=16, num_ranks=4, hidden=256,
+                num_max_tokens_per_rank=32, expert_alignment=8, do_expand=True,
+                do_zero_padding=True, do_cpu_sync=True, use_fp8=False)
+    base.update(kw)
+    args = [base.pop(k) for k in ("num_tokens", "num_topk", "num_experts", "num_ranks", "hidden",
+                                  "num_max_tokens_per_rank")]
+    return ep.make_config(*args, **base)
+
+
+@pytest.mark.parametrize("kw,status", [
+    ({}, 0),
+    ({"num_experts": 18}, 1),                       # E % R != 0
+    ({"hidden": 250}, 1),                           # H % 8 != 0
+    ({"use_fp8": True, "hidden": 264}, 1),          # FP8 needs H % 128 == 0
+    ({"use_fp8": True, "hidden": 384}, 0),
+    ({"num_tokens": 129}, 1),                       # T > M * R
+    ({"num_tokens": -1}, 1),
+    ({"num_topk": 0}, 1),
+    ({"num_topk": 33}, 2),                          # beyond EP_MAX_TOPK
+    ({"num_experts": 4096, "num_ranks": 4}, 2),     # beyond EP_MAX_EXPERTS
+    ({"hidden": 65536}, 2),                         # beyond EP_MAX_HIDDEN
+    ({"expert_alignment": 0}, 1),
+    ({"num_max_tokens_per_rank": 0}, 1),
+    ({"num_sms": -3}, 1),
+    ({"cpu_sync_timeout_ms": -1}, 1),
+])
+def test_validate_config(ep, kw, status):
+    assert ep.validate_config(_cfg(ep, **kw)) == status
+
+
+def test_validate_rejects_bad_flags_and_reserved(ep):
+    c = _cfg(ep)
+    c.do_expand = 2
+    assert ep.validate_config(c) == ep.EP_ERR_INVALID_ARG
+    c = _cfg(ep)
+    c.reserved0[1] = 7
+    assert ep.validate_config(c) == ep.EP_ERR_INVALID_ARG
+    c = _cfg(ep)
+    c.topk_idx_is_int64 = 5
+    assert ep.validate_config(c) == ep.EP_ERR_INVALID_ARG
+    assert ep.load_library().ep_validate_config(None) == ep.EP_ERR_INVALID_ARG
+
+
+def test_upper_bound_rows_match_oracle(ep):
+    rng = np.random.default_rng(3)
+    for _ in range(300):
+        R = int(rng.choice([1, 2, 4, 8, 32]))
+        E = R * int(rng.integers(1, 9))
+        K = int(rng.integers(1, min(E, 32) + 1))
+        M = int(rng.integers(1, 3000))
+        T = int(rng.integers(0, M * R + 1))
+        A = int(rng.choice([1, 2, 8, 128]))
+        for de in (False, True):
+            c = ep.make_config(T, K, E, R, 128, M, A, de)
+            assert ep.upper_bound_rows(c) == O.upper_bound_rows(T, K, E, R, M, A, de)
+
+
+def test_host_wait_flag_deadline(ep):
+    flag = ctypes.c_int32(0)
+    t0 = time.perf_counter()
+    assert ep.host_wait_flag(flag, 1, 80) == ep.EP_ERR_TIMEOUT      # nothing sets it
+    el = time.perf_counter() - t0
+    assert 0.07 <= el < 2.0
+    flag.value = 9
+    assert ep.host_wait_flag(flag, 9, 80) == ep.EP_OK
+    assert ep.load_library().ep_host_wait_flag(None, 1, 10) == ep.EP_ERR_INVALID_ARG
+    assert ep.host_wait_flag(flag, 9, -1) == ep.EP_ERR_INVALID_ARG
+
+
+def test_entry_points_reject_bad_arguments_before_any_cuda_call(ep):
+    lib = ep.load_library()
+    info = ep.EpLayoutInfoC()
+    h = ctypes.c_void_p(0)
+    # missing outputs, bad config, missing topk_idx: refused on the host
+    assert lib.ep_layout(ctypes.byref(_cfg(ep)), None, None, None, ctypes.byref(info)) == 1
+    assert lib.ep_layout(ctypes.byref(_cfg(ep, num_experts=18)), None, None, ctypes.byref(h),
+                         ctypes.byref(info)) == 1
+    assert lib.ep_layout(ctypes.byref(_cfg(ep)), None, None, ctypes.byref(h),
+                         ctypes.byref(info)) == 1
+    assert lib.ep_layout(ctypes.byref(_cfg(ep)), ctypes.c_void_p(0x1003), None, ctypes.byref(h),
+                         ctypes.byref(info)) == 1                  # misaligned int64 topk_idx
+    assert h.value is None
+    assert lib.ep_dispatch(None, None, None, None, None, None, None, None) == 1
+    assert lib.ep_combine(None, None, None, None, None, None, None, None) == 1
+    lib.ep_handle_free(None)
+
+
+def test_status_strings(ep):
+    for code in range(8):
+        s = ep.status_string(code)
+        assert s and s != "unknown status"
+    assert ep.status_string(99) == "unknown status"

@@ -11,4 +11,5 @@ from ._binding import (  # noqa: F401
     EP_ERRBIT_OVERFLOW, EP_OK, LIB_PATH, EpConfigC, EpError, EpLayoutInfoC, Handle,
     alloc_recv, ep_combine, ep_dispatch, ep_handle_free, ep_layout, host_wait_flag,
     load_library, make_config, status_string, upper_bound_rows, validate_config,
+    EP_NOALLOC_SCRATCH_WORDS, EpLayoutBuffersC, alloc_layout_buffers, ep_layout_noalloc,
 )

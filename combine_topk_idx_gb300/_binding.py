@@ -342,3 +342,52 @@ def ep_handle_free(handle: Handle) -> None:
 
 def host_wait_flag(flag: ctypes.c_int32, expected: int, timeout_ms: int) -> int:
     return load_library().ep_host_wait_flag(ctypes.byref(flag), expected, timeout_ms)
+
+
+class EpLayoutBuffersC(ctypes.Structure):
+    _fields_ = [(n, ctypes.c_void_p) for n in (
+        "topk_idx32", "cnt_expert", "cnt_expert_aligned", "psum_expert", "psum_padding",
+        "cnt_rank", "psum_rank", "psum_rank_src", "dst_buffer_slot_idx", "recv_src_metadata",
+        "is_token_in_rank", "status")]
+
+
+EP_NOALLOC_SCRATCH_WORDS = 512 * 1024
+
+
+def alloc_layout_buffers(cfg: EpConfigC, device="cuda") -> dict:
+    """torch-allocated output buffers for ep_layout_noalloc (allocated by the caller)."""
+    T, K, E, R = cfg.num_tokens, cfg.num_topk, cfg.num_experts, cfg.num_ranks
+    rows = upper_bound_rows(cfg)
+    i32 = dict(dtype=torch.int32, device=device)
+    return {
+        "topk_idx32": torch.empty((T, K), **i32),
+        "cnt_expert": torch.empty((E,), **i32),
+        "cnt_expert_aligned": torch.empty((E,), **i32),
+        "psum_expert": torch.empty((E + 1,), **i32),
+        "psum_padding": torch.empty((E + 1,), **i32),
+        "cnt_rank": torch.empty((R,), **i32),
+        "psum_rank": torch.empty((R + 1,), **i32),
+        "psum_rank_src": torch.empty((R, R + 1), **i32),
+        "dst_buffer_slot_idx": torch.empty((T, K), **i32),
+        "recv_src_metadata": torch.empty((rows, 2), **i32),
+        "is_token_in_rank": torch.empty((T, R), dtype=torch.uint8, device=device),
+        "status": torch.empty((4,), **i32),
+    }
+
+
+def ep_layout_noalloc(cfg: EpConfigC, topk_idx: torch.Tensor, buffers: dict, stream=None) -> int:
+    """Allocation-free layout into caller buffers; returns the ep_status code."""
+    lib = load_library()
+    fn = lib.ep_layout_noalloc
+    fn.argtypes = [ctypes.POINTER(EpConfigC), ctypes.c_void_p, ctypes.POINTER(EpLayoutBuffersC),
+                   ctypes.c_void_p]
+    fn.restype = ctypes.c_int
+    if topk_idx.dtype not in (torch.int64, torch.int32):
+        raise ValueError("topk_idx must be int64 or int32")
+    cfg.topk_idx_is_int64 = 1 if topk_idx.dtype == torch.int64 else 0
+    b = EpLayoutBuffersC()
+    for name, _ in EpLayoutBuffersC._fields_:
+        t = buffers.get(name)
+        setattr(b, name, None if t is None or t.numel() == 0 else t.data_ptr())
+    p = topk_idx.data_ptr() if topk_idx.numel() > 0 else None
+    return fn(ctypes.byref(cfg), p, ctypes.byref(b), _stream_ptr(stream))

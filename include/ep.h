@@ -203,6 +203,60 @@ EP_API ep_status ep_combine(const ep_handle *h, const void *y, const float *topk
  */
 EP_API void ep_handle_free(ep_handle *h);
 
+/* ---- layout without any allocation ------------------------------------- */
+
+/*
+ * Caller-owned device buffers that ep_layout_noalloc fills.  Shapes as in
+ * ep_layout_info; `rows` = ep_upper_bound_rows(cfg).
+ */
+typedef struct ep_layout_buffers {
+  int32_t *topk_idx32;           /* [T, K] int32 copy, invalid values -> -1 */
+  int32_t *cnt_expert;           /* [E] */
+  int32_t *cnt_expert_aligned;   /* [E] */
+  int32_t *psum_expert;          /* [E+1] */
+  int32_t *psum_padding;         /* [E+1] exclusive prefix of the padding rows per expert */
+  int32_t *cnt_rank;             /* [R] */
+  int32_t *psum_rank;            /* [R+1] */
+  int32_t *psum_rank_src;        /* [R, R+1] */
+  int32_t *dst_buffer_slot_idx;  /* [T, K] */
+  int32_t *recv_src_metadata;    /* [rows, 2] */
+  uint8_t *is_token_in_rank;     /* [T, R] */
+  int32_t *status;               /* [4]: EP_ERRBIT_* bits, unused, num_recv_tokens,
+                                    num_expanded_tokens */
+} ep_layout_buffers;
+
+/* Largest scratch ep_layout_noalloc can use: 2 MiB of int32 words. */
+#define EP_NOALLOC_SCRATCH_WORDS (512 * 1024)
+
+/*
+ * ep_layout_noalloc -- the routing layout of ep_layout, for callers that may
+ * not allocate memory while they run: code inside a CUDA-graph capture that
+ * must not add allocation nodes, allocator-free inference runtimes that own
+ * every byte of device memory up front, or hosts whose allocator is not
+ * thread-safe at that point.  The pages have no counterpart of this entry
+ * point: it is an allocation-free variant of the layout kernels only.
+ *
+ * It computes exactly what ep_layout computes with do_cpu_sync = 0 and
+ * writes it to the caller's buffers `out` (all device memory, all required);
+ * no handle is created and nothing is allocated (no cudaMalloc, cudaFree or
+ * pool call).  The per-chunk histograms the layout needs live in one static
+ * device array of EP_NOALLOC_SCRATCH_WORDS int32 words that every GPU loading
+ * this library holds until the process exits.  A problem needing more,
+ * chunks * (E + R + 1) words with chunks = ceil(T / M) * ceil(min(M, T) /
+ * 256), is rejected with EP_ERR_UNSUPPORTED before any GPU work;
+ * cfg->do_cpu_sync = 1 is rejected with EP_ERR_INVALID_ARG.
+ *
+ * The first call on a device looks up the array's device address (once per
+ * device, with that device current); make that first call before any stream
+ * capture.  Every call uses the same array and leaves its last contents
+ * there; every word a call reads is written by the same call first, so
+ * nothing has to be cleared between calls.  Calls that overlap on the GPU
+ * (concurrent streams, or several host threads) race on the array: order
+ * them on one stream or with events.
+ */
+EP_API ep_status ep_layout_noalloc(const ep_config *cfg, const void *topk_idx,
+                                   const ep_layout_buffers *out, ep_stream_t stream);
+
 /* ---- host-only helpers (no GPU needed) ---------------------------------- */
 
 /* Human-readable name of a status code (static string). */

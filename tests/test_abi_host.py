@@ -59,10 +59,11 @@ def test_struct_layout_matches_c_header(ep):
 int main(void) {
   printf("ep_config size %zu\n", sizeof(ep_config));
   printf("ep_layout_info size %zu\n", sizeof(ep_layout_info));
+  printf("ep_layout_buffers size %zu\n", sizeof(ep_layout_buffers));
   P(ep_config, num_tokens) P(ep_config, topk_idx_is_int64) P(ep_config, do_expand)
   P(ep_config, use_tma_aligned_col_major_sf) P(ep_config, num_sms) P(ep_config, cpu_sync_timeout_ms)
   P(ep_layout_info, rows_alloc) P(ep_layout_info, topk_idx) P(ep_layout_info, error_word)
-  P(ep_layout_info, meta_rows)
+  P(ep_layout_info, meta_rows) P(ep_layout_buffers, status)
   return 0;
 }
 '''
@@ -77,14 +78,16 @@ int main(void) {
         if ln:
             a, b, v = ln.split()
             got[(a, b)] = int(v)
-    C, I = ep.EpConfigC, ep.EpLayoutInfoC
+    C, I, B = ep.EpConfigC, ep.EpLayoutInfoC, ep.EpLayoutBuffersC
     assert got[("ep_config", "size")] == ctypes.sizeof(C)
     assert got[("ep_layout_info", "size")] == ctypes.sizeof(I)
+    assert got[("ep_layout_buffers", "size")] == ctypes.sizeof(B)
     for f in ("num_tokens", "topk_idx_is_int64", "do_expand", "use_tma_aligned_col_major_sf",
               "num_sms", "cpu_sync_timeout_ms"):
         assert got[("ep_config", f)] == getattr(C, f).offset, f
     for f in ("rows_alloc", "topk_idx", "error_word", "meta_rows"):
         assert got[("ep_layout_info", f)] == getattr(I, f).offset, f
+    assert got[("ep_layout_buffers", "status")] == B.status.offset
 
 
 def _cfg(ep, **kw):
@@ -173,6 +176,19 @@ def test_entry_points_reject_bad_arguments_before_any_cuda_call(ep):
     assert lib.ep_dispatch(None, None, None, None, None, None, None, None) == 1
     assert lib.ep_combine(None, None, None, None, None, None, None, None) == 1
     lib.ep_handle_free(None)
+    # allocation-free layout: sync mode, missing buffers, oversized problems
+    b = ep.EpLayoutBuffersC()
+    fn = lib.ep_layout_noalloc
+    fn.argtypes = [ctypes.POINTER(ep.EpConfigC), ctypes.c_void_p,
+                   ctypes.POINTER(ep.EpLayoutBuffersC), ctypes.c_void_p]
+    assert fn(ctypes.byref(_cfg(ep)), ctypes.c_void_p(0x1000), ctypes.byref(b), None) == 1
+    assert fn(ctypes.byref(_cfg(ep, do_cpu_sync=False)), ctypes.c_void_p(0x1000),
+              ctypes.byref(b), None) == 1
+    for n, _ in ep.EpLayoutBuffersC._fields_:
+        setattr(b, n, 0x10000)
+    T = 256 * 300
+    big = ep.make_config(T, 8, 2048, 16, 128, T // 16 + 1, 1, True, False, False)
+    assert fn(ctypes.byref(big), ctypes.c_void_p(0x1000), ctypes.byref(b), None) == 2
 
 
 def test_status_strings(ep):

@@ -8,16 +8,18 @@
 // Work unit = (token, chunk of the hidden dimension).  Persistent CTAs, warp
 // specialised:
 //   warp 0 (producer) reads a unit's routing (destination rows, weights,
-//     expert ids; prefetched one unit ahead), compacts the valid slots
+//     expert ids; prefetched four units ahead), compacts the valid slots
 //     (dropping repeated rows when there are no weights) and issues one
-//     cp.async.bulk global->shared copy per slot row chunk (plus the expert-
-//     bias and per-token bias chunks) into a ring of kStages shared-memory
-//     stages, completion counted on the stage's "full" mbarrier;
-//   the other warps (consumers) wait for a stage, accumulate its rows
-//     strictly in slot order with separately rounded fp32 multiplies and adds
-//     (__fmul_rn / __fadd_rn: no FMA contraction), add the biases, round to
-//     BF16 (nearest even), store the output chunk, and release the stage on
-//     its "empty" mbarrier.
+//     cp.async.bulk global->shared copy per slot row chunk (plus the per-token
+//     bias chunks) into a ring of kStages shared-memory stages, completion
+//     counted on the stage's "full" mbarrier;
+//   the other warps (consumers) wait for a stage and accumulate its rows
+//     strictly in slot order -- per-expert bias added to each row first (a
+//     small table reused by every token: read through L1, not staged), then
+//     separately rounded fp32 multiplies and adds (__fmul_rn / __fadd_rn: no
+//     FMA contraction) -- add the per-token biases, round to BF16 (nearest
+//     even), store the output chunk and release the stage on its "empty"
+//     mbarrier.
 // Each output element is written by exactly one thread: no atomics.  Every
 // mbarrier wait is bounded; a wait that gives up sets EP_ERRBIT_TIMEOUT in
 // the handle's error word and the CTA returns.
@@ -36,6 +38,7 @@ constexpr uint32_t kWaitHintNs = 500000;
 
 struct StageMeta {
   float w[EP_MAX_TOPK];
+  int e[EP_MAX_TOPK];
   int n;      // valid slots in this unit
 };
 
@@ -132,7 +135,7 @@ __global__ void __launch_bounds__(kMaxConsumers + 32, 1)
       if (use) meta[s].w[pos] = cur.w;
       if (lane == 0) meta[s].n = n;
       __syncwarp();
-      const int rows = n * (HAS_EB ? 2 : 1) + has_b0 + has_b1;
+      const int rows = n + has_b0 + has_b1;
       if (lane == 0) {
         if (rows > 0)
           mbar_arrive_expect_tx(&full[s], (uint32_t)rows * bytes);
@@ -145,12 +148,9 @@ __global__ void __launch_bounds__(kMaxConsumers + 32, 1)
         bulk_load_g2s_hint(sb + (int64_t)pos * chunk_bytes,
                            reinterpret_cast<const uint8_t *>(p.y) + (int64_t)cur.d * row_bytes + off,
                            bytes, &full[s], stream_pol);
-        if (HAS_EB)
-          bulk_load_g2s(sb + (int64_t)(n + pos) * chunk_bytes,
-                        reinterpret_cast<const uint8_t *>(p.ebias) + (int64_t)cur.e * row_bytes + off,
-                        bytes, &full[s]);
+        if (HAS_EB) meta[s].e[pos] = cur.e;
       }
-      const int brow = n * (HAS_EB ? 2 : 1);
+      const int brow = n;
       if (lane == 0 && has_b0)
         bulk_load_g2s(sb + (int64_t)brow * chunk_bytes,
                       reinterpret_cast<const uint8_t *>(p.bias0) + t * row_bytes + off, bytes,
@@ -188,7 +188,7 @@ __global__ void __launch_bounds__(kMaxConsumers + 32, 1)
         unpack8(*reinterpret_cast<const uint4 *>(sb + (int64_t)j * chunk_bytes + v * 16), f);
         if (HAS_EB) {
           float b[8];
-          unpack8(*reinterpret_cast<const uint4 *>(sb + (int64_t)(n + j) * chunk_bytes + v * 16), b);
+          unpack8(ld_cached_v4(p.ebias + (int64_t)meta[s].e[j] * H + off / 2 + v * 8), b);
 #pragma unroll
           for (int q = 0; q < 8; ++q) f[q] = __fadd_rn(f[q], b[q]);
         }
@@ -201,7 +201,7 @@ __global__ void __launch_bounds__(kMaxConsumers + 32, 1)
           for (int q = 0; q < 8; ++q) acc[q] = __fadd_rn(acc[q], f[q]);
         }
       }
-      const int brow = n * (HAS_EB ? 2 : 1);
+      const int brow = n;
       for (int b = 0; b < has_b0 + has_b1; ++b) {
         float f[8];
         unpack8(*reinterpret_cast<const uint4 *>(sb + (int64_t)(brow + b) * chunk_bytes + v * 16), f);
@@ -225,7 +225,7 @@ cudaError_t launch_one(const CombineParams &p, int sm_cap, cudaStream_t s) {
   auto kern = combine_kernel<W, EB>;
   const int64_t row_bytes = 2 * (int64_t)p.H;
   const int nbias = (p.bias0 != nullptr) + (p.bias1 != nullptr);
-  const int slots_cap = p.K * (EB ? 2 : 1) + nbias;
+  const int slots_cap = p.K + nbias;
   // Stage budget ~96 KB per CTA (two CTAs per SM); chunks are equal-sized
   // multiples of 16 bytes.
   const int64_t budget = 96 * 1024 / kStages;

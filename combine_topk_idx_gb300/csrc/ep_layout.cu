@@ -81,6 +81,31 @@ __device__ int cta_exclusive_scan(int n, F f, int32_t *out, int *warp_tot) {
   return total;
 }
 
+// Exclusive scan of f(i), i < n, by one warp into out[0..n]; returns the total.
+template <typename F>
+__device__ int warp_exclusive_scan(int n, F f, int32_t *out) {
+  const int lane = threadIdx.x & 31;
+  const int per = (n + 31) / 32;
+  const int beg = min(lane * per, n);
+  const int end = min(beg + per, n);
+  int local = 0;
+  for (int i = beg; i < end; ++i) local += f(i);
+  int incl = local;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const int v = __shfl_up_sync(0xffffffffu, incl, o);
+    if (lane >= o) incl += v;
+  }
+  int run = incl - local;
+  for (int i = beg; i < end; ++i) {
+    out[i] = run;
+    run += f(i);
+  }
+  const int total = __shfl_sync(0xffffffffu, incl, 31);
+  if (lane == 0) out[n] = total;
+  return total;
+}
+
 __global__ void __launch_bounds__(NTC) layout_count_kernel(LayoutParams p) {
   extern __shared__ __align__(16) int smem[];
   const int K = p.K, L = p.L, R = p.R, E = p.E;
@@ -196,29 +221,45 @@ __global__ void __launch_bounds__(NT) layout_assign_kernel(LayoutParams p) {
   for (int i = threadIdx.x; i < ns; i += NT) idx_s[i] = p.topk32[base + i];
   for (int i = threadIdx.x; i < nrw * nkey; i += NT) whist[i] = 0ull;
   for (int e = threadIdx.x; e < E; e += NT) rank_of[e] = e / L;
-  // Column sums of the per-chunk histograms: global totals and this chunk's offset.
-  for (int key = threadIdx.x; key < E + R; key += NT) {
-    const int32_t *col = key < E ? p.blk_e + key : p.blk_r + (key - E);
-    const int stride = key < E ? E : R;
-    int tot = 0, bef = 0;
-    int bb = 0;
-    for (; bb + 16 <= p.num_blocks; bb += 16) {
-      int v[16];
+  // Column sums of the per-chunk histograms: global totals and this chunk's
+  // offset.  g consecutive lanes share a key and split its chunks.
+  {
+    const int nk = E + R;
+    int g = 1;
+    while (g < 32 && g * 2 * nk <= NT) g <<= 1;
+    const int sub = threadIdx.x & (g - 1);
+    for (int key = threadIdx.x / g; key < nk + (NT / g - 1) - (nk + NT / g - 1) % (NT / g);
+         key += NT / g) {
+      int tot = 0, bef = 0;
+      if (key < nk) {
+        const int32_t *col = key < E ? p.blk_e + key : p.blk_r + (key - E);
+        const int stride = key < E ? E : R;
+        int bb = sub;
+        for (; bb + 7 * g < p.num_blocks; bb += 8 * g) {
+          int v[8];
 #pragma unroll
-      for (int u = 0; u < 16; ++u) v[u] = __ldcg(col + (int64_t)(bb + u) * stride);
+          for (int u = 0; u < 8; ++u) v[u] = __ldcg(col + (int64_t)(bb + u * g) * stride);
 #pragma unroll
-      for (int u = 0; u < 16; ++u) {
-        tot += v[u];
-        bef += (bb + u < b) ? v[u] : 0;
+          for (int u = 0; u < 8; ++u) {
+            tot += v[u];
+            bef += (bb + u * g < b) ? v[u] : 0;
+          }
+        }
+        for (; bb < p.num_blocks; bb += g) {
+          const int v = __ldcg(col + (int64_t)bb * stride);
+          tot += v;
+          bef += (bb < b) ? v : 0;
+        }
+      }
+      for (int o = g >> 1; o > 0; o >>= 1) {
+        tot += __shfl_xor_sync(0xffffffffu, tot, o);
+        bef += __shfl_xor_sync(0xffffffffu, bef, o);
+      }
+      if (key < nk && sub == 0) {
+        tot_s[key] = tot;
+        bef_s[key] = bef;
       }
     }
-    for (; bb < p.num_blocks; ++bb) {
-      const int v = __ldcg(col + (int64_t)bb * stride);
-      tot += v;
-      bef += (bb < b) ? v : 0;
-    }
-    tot_s[key] = tot;
-    bef_s[key] = bef;
   }
   __syncthreads();
 
@@ -229,69 +270,76 @@ __global__ void __launch_bounds__(NT) layout_assign_kernel(LayoutParams p) {
     cta_exclusive_scan(R, [&](int r) { return tot_s[E + r]; }, seg_s, warp_tot);
 
   if (b == 0) {
-    // Global outputs (written once, by CTA 0).  The sort key's prefix sum is
-    // seg_s already; the other one and the padding prefix take one scan each.
+    // Global outputs, written once by CTA 0.  The sort key's prefix sum is
+    // seg_s already; the rest is split over warps so it adds one short phase:
+    // warp 0 the other prefix sum, the error bits and the totals (then the
+    // host notification), warp 1 the padding prefix, the other warps the
+    // per-source-rank prefixes.
     for (int e = threadIdx.x; e < E; e += NT) {
       p.cnt_e[e] = tot_s[e];
       p.cnt_e_al[e] = (tot_s[e] + A - 1) / A * A;
     }
     for (int r = threadIdx.x; r < R; r += NT) p.cnt_r[r] = tot_s[E + r];
-    int num_expanded, num_recv;
     if (p.do_expand) {
       for (int e = threadIdx.x; e <= E; e += NT) p.psum_e[e] = seg_s[e];
-      num_expanded = seg_s[E];
-      num_recv = cta_exclusive_scan(R, [&](int r) { return tot_s[E + r]; }, p.psum_r, warp_tot);
     } else {
       for (int r = threadIdx.x; r <= R; r += NT) p.psum_r[r] = seg_s[r];
-      num_recv = seg_s[R];
-      num_expanded = cta_exclusive_scan(E, [&](int e) { return (tot_s[e] + A - 1) / A * A; },
-                                        p.psum_e, warp_tot);
     }
-    cta_exclusive_scan(E, [&](int e) { return (tot_s[e] + A - 1) / A * A - tot_s[e]; }, p.psum_pad,
-                       warp_tot);
-    unsigned err = 0;
-    for (int bb = threadIdx.x; bb < p.num_blocks; bb += NT) err |= __ldcg(p.blk_err + bb);
-    err = __reduce_or_sync(0xffffffffu, err);
-    if (lane == 0) warp_tot[warp] = static_cast<int>(err);
-    __syncthreads();
-    if (threadIdx.x == 0) {
-      for (int w = 1; w < NWARPS; ++w) err |= static_cast<unsigned>(warp_tot[w]);
-      const int64_t total_rows = p.do_expand ? num_expanded : num_recv;
-      if (total_rows > p.row_limit) err |= EP_ERRBIT_OVERFLOW;
-      p.ctrl[kCtrlError] = static_cast<int>(err);
-      p.ctrl[kCtrlNumRecv] = num_recv;
-      p.ctrl[kCtrlNumExpanded] = num_expanded;
-      if (p.host != nullptr) {
-        p.host->error = static_cast<int>(err);
-        p.host->num_recv = num_recv;
-        p.host->num_expanded = num_expanded;
-        __threadfence_system();
-        p.host->flag = p.seq;
+    if (warp == 0) {
+      int num_expanded, num_recv;
+      if (p.do_expand) {
+        num_expanded = seg_s[E];
+        num_recv = warp_exclusive_scan(R, [&](int r) { return tot_s[E + r]; }, p.psum_r);
+      } else {
+        num_recv = seg_s[R];
+        num_expanded =
+            warp_exclusive_scan(E, [&](int e) { return (tot_s[e] + A - 1) / A * A; }, p.psum_e);
       }
-    }
-    // psum_rank_src[r][s]: tokens of source ranks < s received by rank r.
-    // Chunks are ordered by source rank; one warp scans each r over s.
-    const int src_ranks = p.num_blocks / p.blocks_per_src;
-    const int RR = R + 1;
-    for (int r = warp; r < R; r += NWARPS) {
-      int carry = 0;
-      if (lane == 0) p.psum_rs[(int64_t)r * RR] = 0;
-      for (int s0 = 0; s0 < R; s0 += 32) {
-        const int s = s0 + lane;
-        int c = 0;
-        if (s < R && s < src_ranks && p.T > 0) {
-          const int lo = s * p.blocks_per_src;
-          const int hi = min(lo + p.blocks_per_src, p.num_blocks);
-          for (int bb = lo; bb < hi; ++bb) c += __ldcg(p.blk_r + (int64_t)bb * R + r);
+      unsigned err = 0;
+      for (int bb = lane; bb < p.num_blocks; bb += 32) err |= __ldcg(p.blk_err + bb);
+      err = __reduce_or_sync(0xffffffffu, err);
+      if (lane == 0) {
+        const int64_t total_rows = p.do_expand ? num_expanded : num_recv;
+        if (total_rows > p.row_limit) err |= EP_ERRBIT_OVERFLOW;
+        p.ctrl[kCtrlError] = static_cast<int>(err);
+        p.ctrl[kCtrlNumRecv] = num_recv;
+        p.ctrl[kCtrlNumExpanded] = num_expanded;
+        if (p.host != nullptr) {
+          p.host->error = static_cast<int>(err);
+          p.host->num_recv = num_recv;
+          p.host->num_expanded = num_expanded;
+          __threadfence_system();
+          p.host->flag = p.seq;
         }
-        int incl = c;
+      }
+    } else if (warp == 1) {
+      warp_exclusive_scan(E, [&](int e) { return (tot_s[e] + A - 1) / A * A - tot_s[e]; },
+                          p.psum_pad);
+    } else {
+      // psum_rank_src[r][s]: tokens of source ranks < s received by rank r.
+      // Chunks are ordered by source rank; one warp scans each r over s.
+      const int src_ranks = p.num_blocks / p.blocks_per_src;
+      const int RR = R + 1;
+      for (int r = warp - 2; r < R; r += NWARPS - 2) {
+        int carry = 0;
+        if (lane == 0) p.psum_rs[(int64_t)r * RR] = 0;
+        for (int s0 = 0; s0 < R; s0 += 32) {
+          const int s = s0 + lane;
+          int c = 0;
+          if (s < R && s < src_ranks && p.T > 0) {
+            const int lo = s * p.blocks_per_src;
+            const int hi = min(lo + p.blocks_per_src, p.num_blocks);
+            for (int bb = lo; bb < hi; ++bb) c += __ldcg(p.blk_r + (int64_t)bb * R + r);
+          }
+          int incl = c;
 #pragma unroll
-        for (int o = 1; o < 32; o <<= 1) {
-          const int v = __shfl_up_sync(0xffffffffu, incl, o);
-          if (lane >= o) incl += v;
+          for (int o = 1; o < 32; o <<= 1) {
+            const int v = __shfl_up_sync(0xffffffffu, incl, o);
+            if (lane >= o) incl += v;
+          }
+          if (s < R) p.psum_rs[(int64_t)r * RR + s + 1] = carry + incl;
+          carry += __shfl_sync(0xffffffffu, incl, 31);
         }
-        if (s < R) p.psum_rs[(int64_t)r * RR + s + 1] = carry + incl;
-        carry += __shfl_sync(0xffffffffu, incl, 31);
       }
     }
   }

@@ -308,6 +308,7 @@ __global__ void __launch_bounds__(kMaxConsumers + 32, 1) dispatch_kernel(Dispatc
       if (lane == 0) mbar_arrive(&empty[s]);
     }
   }
+  griddep_launch_dependents();
   if (ctid == 0) bulk_wait_all<0>();
 }
 
@@ -316,6 +317,7 @@ __global__ void __launch_bounds__(kMaxConsumers + 32, 1) dispatch_kernel(Dispatc
 // thread per row: 16-byte loads of the token's scales, and for each scale
 // block j the warp writes 32 consecutive rows (coalesced).  Padding rows get 0.
 __global__ void __launch_bounds__(256) sf_expand_kernel(DispatchParams p) {
+  griddep_wait();  // the per-token scales come from the dispatch kernel
   const int nb = p.H / kFp8Block;
   const int64_t total = min((int64_t)__ldg(p.num_rows), p.rows_alloc);
   const int2 *meta = reinterpret_cast<const int2 *>(p.meta);
@@ -375,8 +377,17 @@ cudaError_t launch_one(const DispatchParams &p, int sm_cap, cudaStream_t s) {
   // upper-bound allocation, are left untouched)
   const int64_t sf_grid = std::min<int64_t>((p.rows_alloc + 255) / 256, (int64_t)use_sms * 8);
   if (sf_grid > 0) {
-    sf_expand_kernel<<<(int)sf_grid, 256, 0, s>>>(p);
-    err = cudaGetLastError();
+    // launched while the dispatch kernel drains; it waits on griddepcontrol
+    cudaLaunchConfig_t lc{};
+    lc.gridDim = dim3((unsigned)sf_grid);
+    lc.blockDim = dim3(256);
+    lc.stream = s;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    lc.attrs = attr;
+    lc.numAttrs = 1;
+    err = cudaLaunchKernelEx(&lc, sf_expand_kernel, p);
   }
   return err;
 }

@@ -22,6 +22,7 @@
 #include <algorithm>
 
 #include "ep_internal.cuh"
+#include "ep_ptx.cuh"
 
 namespace ep {
 namespace {
@@ -138,6 +139,7 @@ __global__ void __launch_bounds__(NTC) layout_count_kernel(LayoutParams p) {
   }
   err = __reduce_or_sync(0xffffffffu, err);
   __syncthreads();
+  griddep_launch_dependents();  // the assign kernel's prologue may start now
   if (lane == 0 && err) atomicOr(&err_s, err);
 
   // One thread per token: expert histogram and the token's rank set.
@@ -218,9 +220,10 @@ __global__ void __launch_bounds__(NT) layout_assign_kernel(LayoutParams p) {
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
   const int nrw = p.rank_warps;
 
-  for (int i = threadIdx.x; i < ns; i += NT) idx_s[i] = p.topk32[base + i];
   for (int i = threadIdx.x; i < nrw * nkey; i += NT) whist[i] = 0ull;
   for (int e = threadIdx.x; e < E; e += NT) rank_of[e] = e / L;
+  griddep_wait();  // everything below reads the count kernel's outputs
+  for (int i = threadIdx.x; i < ns; i += NT) idx_s[i] = p.topk32[base + i];
   // Column sums of the per-chunk histograms: global totals and this chunk's
   // offset.  g consecutive lanes share a key and split its chunks.
   {
@@ -477,8 +480,19 @@ cudaError_t launch_layout(const LayoutParams &p, cudaStream_t s) {
   layout_count_kernel<<<p.num_blocks, NTC, smem_count, s>>>(p);
   err = cudaGetLastError();
   if (err != cudaSuccess) return err;
-  layout_assign_kernel<<<p.num_blocks, NT, smem_assign, s>>>(p);
-  return cudaGetLastError();
+  // assign may launch while count drains (programmatic dependent launch); it
+  // waits on griddepcontrol before touching count's outputs
+  cudaLaunchConfig_t lc{};
+  lc.gridDim = dim3(p.num_blocks);
+  lc.blockDim = dim3(NT);
+  lc.dynamicSmemBytes = smem_assign;
+  lc.stream = s;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  lc.attrs = attr;
+  lc.numAttrs = 1;
+  return cudaLaunchKernelEx(&lc, layout_assign_kernel, p);
 }
 
 }  // namespace ep

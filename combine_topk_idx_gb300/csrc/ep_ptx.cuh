@@ -187,3 +187,18 @@ __device__ __forceinline__ void bulk_load_g2s_hint(void *sdst, const void *gsrc,
 }
 
 }  // namespace ep
+
+namespace ep {
+
+// Programmatic dependent launch: a kernel launched with the programmatic
+// stream-serialisation attribute may start while its predecessor drains;
+// griddep_wait() blocks until the predecessor's memory is visible, and
+// griddep_launch_dependents() lets the successor start launching early.
+__device__ __forceinline__ void griddep_wait() {
+  asm volatile("griddepcontrol.wait;" ::: "memory");
+}
+__device__ __forceinline__ void griddep_launch_dependents() {
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+
+}  // namespace ep

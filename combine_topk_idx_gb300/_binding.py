@@ -391,3 +391,16 @@ def ep_layout_noalloc(cfg: EpConfigC, topk_idx: torch.Tensor, buffers: dict, str
         setattr(b, name, None if t is None or t.numel() == 0 else t.data_ptr())
     p = topk_idx.data_ptr() if topk_idx.numel() > 0 else None
     return fn(ctypes.byref(cfg), p, ctypes.byref(b), _stream_ptr(stream))
+
+
+def selftest_bounded_wait(wait_us: int, signal: bool, stream=None) -> int:
+    """Runs the bounded-wait self-test; returns the EP_ERRBIT_* bits it reported."""
+    lib = load_library()
+    fn = lib.ep_selftest_bounded_wait
+    fn.argtypes = [ctypes.c_int32, ctypes.c_int32, ctypes.POINTER(ctypes.c_uint32), ctypes.c_void_p]
+    fn.restype = ctypes.c_int
+    bits = ctypes.c_uint32(0xFFFFFFFF)
+    st = fn(wait_us, 1 if signal else 0, ctypes.byref(bits), _stream_ptr(stream))
+    if st != EP_OK:
+        raise EpError(st, "ep_selftest_bounded_wait")
+    return bits.value

@@ -209,11 +209,10 @@ ep_status ep_layout(const ep_config *cfg, const void *topk_idx, ep_stream_t stre
   if (T > 0 && (topk_idx == nullptr || !aligned(topk_idx, c.topk_idx_is_int64 ? 8 : 4)))
     return EP_ERR_INVALID_ARG;
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
-  if (c.do_cpu_sync) {
-    cudaStreamCaptureStatus cs = cudaStreamCaptureStatusNone;
-    if (cudaStreamIsCapturing(s, &cs) != cudaSuccess) return EP_ERR_CUDA;
-    if (cs != cudaStreamCaptureStatusNone) return EP_ERR_INVALID_ARG;
-  }
+  cudaStreamCaptureStatus cs = cudaStreamCaptureStatusNone;
+  if (cudaStreamIsCapturing(s, &cs) != cudaSuccess) return EP_ERR_CUDA;
+  const bool capturing = cs != cudaStreamCaptureStatusNone;
+  if (c.do_cpu_sync && capturing) return EP_ERR_INVALID_ARG;
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess) return EP_ERR_CUDA;
 
@@ -264,10 +263,15 @@ ep_status ep_layout(const ep_config *cfg, const void *topk_idx, ep_stream_t stre
   const size_t o_blkerr = take(sizeof(uint32_t) * (size_t)lp.num_blocks);
   const size_t o_toks = take(c.use_fp8 ? sizeof(float) * (size_t)T * (c.hidden / ep::kFp8Block) : 0);
   void *dmem = nullptr;
-  cudaMemPool_t pool = nullptr;
-  cudaError_t ce = ep::handle_pool(dev, &pool);
-  if (ce != cudaSuccess) return ep::cuda_status(ce);
-  ce = cudaMallocFromPoolAsync(&dmem, off, pool, s);
+  cudaError_t ce;
+  if (capturing) {
+    // inside a stream capture the allocation becomes a graph memory node
+    ce = cudaMallocAsync(&dmem, off, s);
+  } else {
+    cudaMemPool_t pool = nullptr;
+    ce = ep::handle_pool(dev, &pool);
+    if (ce == cudaSuccess) ce = cudaMallocFromPoolAsync(&dmem, off, pool, s);
+  }
   if (ce != cudaSuccess) return ep::cuda_status(ce);
   uint8_t *base = static_cast<uint8_t *>(dmem);
   lp.ctrl = reinterpret_cast<int32_t *>(base + o_ctrl);

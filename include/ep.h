@@ -257,6 +257,22 @@ typedef struct ep_layout_buffers {
 EP_API ep_status ep_layout_noalloc(const ep_config *cfg, const void *topk_idx,
                                    const ep_layout_buffers *out, ep_stream_t stream);
 
+/* ---- diagnostics -------------------------------------------------------- */
+
+/*
+ * ep_selftest_bounded_wait -- exercises the bounded device-side wait that
+ * every dispatch / combine pipeline stage uses (mbarrier try_wait with a
+ * suspend-time hint, a fixed number of attempts).  One CTA waits on an
+ * mbarrier for at most about `wait_us` microseconds; with `signal` = 0 nothing
+ * ever arrives, so the wait runs out and the kernel reports EP_ERRBIT_TIMEOUT
+ * instead of hanging; with `signal` = 1 the barrier is completed first and
+ * no bit is set.  The bits are written to *error_bits (host pointer) after
+ * the stream has been synchronised.  The CUDA context stays usable either
+ * way.  Not part of the method; used by the failure-detection tests.
+ */
+EP_API ep_status ep_selftest_bounded_wait(int32_t wait_us, int32_t signal,
+                                          uint32_t *error_bits, ep_stream_t stream);
+
 /* ---- host-only helpers (no GPU needed) ---------------------------------- */
 
 /* Human-readable name of a status code (static string). */

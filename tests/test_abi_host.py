@@ -189,6 +189,11 @@ def test_entry_points_reject_bad_arguments_before_any_cuda_call(ep):
     T = 256 * 300
     big = ep.make_config(T, 8, 2048, 16, 128, T // 16 + 1, 1, True, False, False)
     assert fn(ctypes.byref(big), ctypes.c_void_p(0x1000), ctypes.byref(b), None) == 2
+    # bounded-wait self-test: argument checks happen on the host
+    st = lib.ep_selftest_bounded_wait
+    st.argtypes = [ctypes.c_int32, ctypes.c_int32, ctypes.c_void_p, ctypes.c_void_p]
+    assert st(1000, 0, None, None) == 1
+    assert st(0, 0, ctypes.byref(ctypes.c_uint32()), None) == 1
 
 
 def test_status_strings(ep):

@@ -321,3 +321,77 @@ def test_layout_deterministic_and_cached_dispatch(ep):
         HN.check_dispatch(h1, lay, d_or, out, False, False)
     h1.free()
     h2.free()
+
+
+@pytest.mark.parametrize("name,T", [("decode", None), ("large", 2048)])
+def test_cuda_graph_capture_and_replay(ep, name, T):
+    """Without the host count wait the whole path is stream-ordered: capture
+    layout + dispatch + combine (+ handle free) in a CUDA graph, replay it on
+    new inputs copied into the captured buffers, and compare with an eager
+    run of the same inputs."""
+    wl = W.WORKLOADS[name]
+    T = wl.num_tokens if T is None else T
+    cfg = HN.cfg_for(ep, wl, T=T, do_cpu_sync=False)
+    K, H = wl.num_topk, wl.hidden
+    rows = ep.upper_bound_rows(cfg)
+    dev = torch.device("cuda")
+    idx_s = torch.empty((T, K), dtype=torch.int64, device=dev)
+    w_s = torch.empty((T, K), dtype=torch.float32, device=dev)
+    x_s = torch.empty((T, H), dtype=torch.bfloat16, device=dev)
+    y_s = make_y(rows, H, 21, dev)
+    nb = H // 128
+    sfn = O.sf_numel(rows, H, wl.col_major_sf) if wl.use_fp8 else 0
+    recv = {"recv_x": torch.zeros((rows, H), dtype=torch.uint8 if wl.use_fp8 else torch.bfloat16,
+                                  device=dev),
+            "recv_sf": torch.zeros((sfn,), dtype=torch.float32, device=dev) if wl.use_fp8 else None,
+            "recv_topk_weights": torch.zeros((rows,) if wl.do_expand else (rows, K),
+                                             dtype=torch.float32, device=dev)}
+    res = torch.empty((T, H), dtype=torch.bfloat16, device=dev)
+
+    def fill(seed):
+        inp = W.make_inputs(wl, seed, num_tokens=T)
+        idx_s.copy_(inp["topk_idx"])
+        w_s.copy_(inp["topk_weights"])
+        x_s.copy_(inp["x"])
+
+    def path(st):
+        h = ep.ep_layout(cfg, idx_s, stream=st)
+        ep.ep_dispatch(h, x_s, w_s, stream=st, **recv)
+        ep.ep_combine(h, y_s, w_s, out=res, stream=st)
+        h.free()
+
+    s = torch.cuda.Stream()
+    fill(0)
+    s.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(s):
+        path(s)                           # warm-up outside the capture
+    torch.cuda.synchronize()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g, stream=s):
+        path(s)
+    for seed in (7, 8):
+        fill(seed)
+        torch.cuda.synchronize()
+        g.replay()
+        torch.cuda.synchronize()
+        got = {k: v.clone() for k, v in recv.items() if v is not None}
+        got_res = res.clone()
+        h = ep.ep_layout(cfg, idx_s)
+        total = int(h.tensor("totals").cpu()[1 if wl.do_expand else 0])
+        eager = ep.alloc_recv(h, with_weights=True)
+        ep.ep_dispatch(h, x_s, w_s, **eager)
+        ref = ep.ep_combine(h, y_s, w_s)
+        torch.cuda.synchronize()
+        assert torch.equal(got["recv_x"][:total], eager["recv_x"][:total])
+        if wl.use_fp8:
+            if wl.col_major_sf:
+                st = -(-rows // 4) * 4
+                a = got["recv_sf"].view(nb, st)[:, :total]
+                b = eager["recv_sf"].view(nb, st)[:, :total]
+            else:
+                a = got["recv_sf"].view(rows, nb)[:total]
+                b = eager["recv_sf"].view(rows, nb)[:total]
+            assert torch.equal(a, b)
+        assert torch.equal(got["recv_topk_weights"][:total], eager["recv_topk_weights"][:total])
+        assert torch.equal(got_res, ref)
+        h.free()

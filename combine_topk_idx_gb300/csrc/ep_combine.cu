@@ -132,7 +132,10 @@ __global__ void __launch_bounds__(kMaxConsumers + 32, 1)
       const unsigned m = __ballot_sync(0xffffffffu, use);
       const int n = __popc(m);
       const int pos = __popc(m & lanemask_lt());
-      if (use) meta[s].w[pos] = cur.w;
+      if (use) {
+        meta[s].w[pos] = cur.w;
+        if (HAS_EB) meta[s].e[pos] = cur.e;
+      }
       if (lane == 0) meta[s].n = n;
       __syncwarp();
       const int rows = n + has_b0 + has_b1;
@@ -148,7 +151,6 @@ __global__ void __launch_bounds__(kMaxConsumers + 32, 1)
         bulk_load_g2s_hint(sb + (int64_t)pos * chunk_bytes,
                            reinterpret_cast<const uint8_t *>(p.y) + (int64_t)cur.d * row_bytes + off,
                            bytes, &full[s], stream_pol);
-        if (HAS_EB) meta[s].e[pos] = cur.e;
       }
       const int brow = n;
       if (lane == 0 && has_b0)

@@ -313,31 +313,33 @@ __global__ void __launch_bounds__(kMaxConsumers + 32, 1) dispatch_kernel(Dispatc
 }
 
 // Column-major scale factors of every destination row, gathered from the
-// per-token scales through the row's source token (recv_src_metadata).  One
-// thread per row: 16-byte loads of the token's scales, and for each scale
-// block j the warp writes 32 consecutive rows (coalesced).  Padding rows get 0.
+// per-token scales through the row's source token (recv_src_metadata).  Grid
+// (row blocks, groups of 4 scale blocks): thread (row, g) loads 16 bytes of
+// its token's scales and writes scale blocks 4g..4g+3 of its row, so for
+// each block the threads of a warp write 32 consecutive rows.  Padding rows
+// get 0.
 __global__ void __launch_bounds__(256) sf_expand_kernel(DispatchParams p) {
   griddep_wait();  // the per-token scales come from the dispatch kernel
   const int nb = p.H / kFp8Block;
   const int64_t total = min((int64_t)__ldg(p.num_rows), p.rows_alloc);
-  const int2 *meta = reinterpret_cast<const int2 *>(p.meta);
-  for (int64_t row = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; row < total;
-       row += (int64_t)gridDim.x * blockDim.x) {
-    const int tok = __ldg(&meta[row].x);
-    const float *src = p.tok_scale + (int64_t)(tok >= 0 ? tok : 0) * nb;
-    float *dst = p.recv_sf + row;
-    int j = 0;
+  const int64_t row = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
+  if (row >= total) return;
+  const int j0 = blockIdx.y * 4;
+  const int tok = __ldg(&reinterpret_cast<const int2 *>(p.meta)[row].x);
+  float v[4] = {0.f, 0.f, 0.f, 0.f};
+  if (tok >= 0) {
+    const float *src = p.tok_scale + (int64_t)tok * nb + j0;
     if ((nb & 3) == 0) {
-      for (; j < nb; j += 4) {
-        float4 v = tok >= 0 ? __ldg(reinterpret_cast<const float4 *>(src + j)) : make_float4(0, 0, 0, 0);
-        dst[(int64_t)j * p.sf_hidden_stride] = v.x;
-        dst[(int64_t)(j + 1) * p.sf_hidden_stride] = v.y;
-        dst[(int64_t)(j + 2) * p.sf_hidden_stride] = v.z;
-        dst[(int64_t)(j + 3) * p.sf_hidden_stride] = v.w;
-      }
+      const float4 q = __ldg(reinterpret_cast<const float4 *>(src));
+      v[0] = q.x; v[1] = q.y; v[2] = q.z; v[3] = q.w;
+    } else {
+      for (int u = 0; u < 4 && j0 + u < nb; ++u) v[u] = __ldg(src + u);
     }
-    for (; j < nb; ++j) dst[(int64_t)j * p.sf_hidden_stride] = tok >= 0 ? __ldg(src + j) : 0.f;
   }
+  float *dst = p.recv_sf + row + (int64_t)j0 * p.sf_hidden_stride;
+#pragma unroll
+  for (int u = 0; u < 4; ++u)
+    if (j0 + u < nb) dst[(int64_t)u * p.sf_hidden_stride] = v[u];
 }
 
 template <bool FP8, bool CM>
@@ -375,11 +377,12 @@ cudaError_t launch_one(const DispatchParams &p, int sm_cap, cudaStream_t s) {
   if (err != cudaSuccess || !FP8 || !CM) return err;
   // column-major scales: one gather pass (rows past the real total, in an
   // upper-bound allocation, are left untouched)
-  const int64_t sf_grid = std::min<int64_t>((p.rows_alloc + 255) / 256, (int64_t)use_sms * 8);
+  const int64_t sf_grid = (p.rows_alloc + 255) / 256;
+  const int groups = (H / kFp8Block + 3) / 4;
   if (sf_grid > 0) {
     // launched while the dispatch kernel drains; it waits on griddepcontrol
     cudaLaunchConfig_t lc{};
-    lc.gridDim = dim3((unsigned)sf_grid);
+    lc.gridDim = dim3((unsigned)sf_grid, (unsigned)groups);
     lc.blockDim = dim3(256);
     lc.stream = s;
     cudaLaunchAttribute attr[1];

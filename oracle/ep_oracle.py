@@ -44,7 +44,7 @@ import numpy as np
 __all__ = [
     "align", "upper_bound_rows", "layout", "bf16_bits_to_f32", "f32_to_bf16_bits",
     "e4m3_encode", "e4m3_decode", "quantize_row", "dispatch", "combine",
-    "sf_numel", "sf_index", "FP8_BLOCK", "E4M3_MAX",
+    "sf_numel", "sf_index", "FP8_BLOCK", "E4M3_MAX", "combine_topk_weights",
 ]
 
 FP8_BLOCK = 128        # 1x128 per-row scale blocks
@@ -445,3 +445,44 @@ def combine(lay, y_bits, topk_weights=None, bias_0=None, bias_1=None,
     if bias_1 is not None:
         acc = (acc + bf16_bits_to_f32(np.asarray(bias_1)[tokens])).astype(np.float32)
     return f32_to_bf16_bits(acc)
+
+
+# --------------------------------------------------------------------------
+# Backward pair -- DeepEP README, "Interfaces and examples" (dispatch_backward
+# is a combine of the received gradients together with their top-k weights;
+# combine_backward is a dispatch of the combined gradient)
+# --------------------------------------------------------------------------
+def combine_topk_weights(lay, recv_topk_weights):
+    """Reduction that combine applies to per-row top-k weights.
+
+    The backward of dispatch is a combine that also carries the gradient of
+    the received weights back to token order (DeepEP README, "Interfaces and
+    examples", ``dispatch_backward``).  Reading R17: combine reduces the
+    weights the way it reduces unweighted data -- a plain fp32 sum over the
+    token's distinct destination rows, in the order the rows first appear in
+    its slots.  Expanded layout: one scalar per row, and each row belongs to
+    one slot, so slot k gets its own row's value (0 when the slot has no
+    row).  Rank layout: ``recv_topk_weights`` is [rows, K]; the token's
+    result is the sum of its rows' K-vectors, every column (0 for a token
+    without rows).
+    """
+    dst = lay["dst_buffer_slot_idx"]
+    T, K = dst.shape
+    g = np.asarray(recv_topk_weights, dtype=np.float32)
+    out = np.zeros((T, K), dtype=np.float32)
+    for t in range(T):
+        if lay["do_expand"]:
+            for k in range(K):
+                if dst[t, k] >= 0:
+                    out[t, k] = g[dst[t, k]]
+            continue
+        seen = []
+        for k in range(K):
+            r = int(dst[t, k])
+            if r >= 0 and r not in seen:
+                seen.append(r)
+        acc = np.zeros(K, dtype=np.float32)
+        for r in seen:
+            acc = (acc + g[r]).astype(np.float32)
+        out[t] = acc
+    return out

@@ -589,3 +589,82 @@ def test_planted_quant_mistakes_are_caught(kind):
 def test_planted_combine_mistakes_are_caught(kind):
     with pytest.raises(AssertionError):
         check_combine_fp64(_mutant_combine(kind), 0)
+
+
+# ---------------------------------------------------------------------------
+# Backward pair: dispatch and combine are adjoint; the weight reduction
+# ---------------------------------------------------------------------------
+def _routing(rng, T, K, E, dup):
+    if dup:
+        return rng.integers(-1, E, (T, K))
+    idx = np.array([rng.permutation(E)[:K] for _ in range(T)])
+    idx[rng.random((T, K)) < 0.2] = -1
+    return idx
+
+
+@pytest.mark.parametrize("de", [True, False])
+@pytest.mark.parametrize("dup", [False, True])
+def test_unweighted_combine_is_the_adjoint_of_dispatch(de, dup):
+    """<dispatch(x), g> == <x, combine(g)> exactly: with small integer values
+    every sum is exact in fp32 and BF16, so any wrong row, dropped slot or
+    double-counted shared row breaks the identity."""
+    rng = np.random.default_rng(41 + de + 2 * dup)
+    T, K, E, R, H = 70, 6, 16, 4, 24
+    idx = _routing(rng, T, K, E, dup)
+    lay = O.layout(idx, E, R, 18, 4, de, True)
+    rows = lay["rows_alloc"]
+    x = rng.integers(-2, 3, (T, H)).astype(np.float32)
+    g = rng.integers(-2, 3, (rows, H)).astype(np.float32)
+    d = O.dispatch(lay, O.f32_to_bf16_bits(x), None, do_zero_padding=True)
+    dx = O.bf16_bits_to_f32(d["recv_x"]).astype(np.float64)
+    back = O.bf16_bits_to_f32(O.combine(lay, O.f32_to_bf16_bits(g))).astype(np.float64)
+    lhs = float((dx * g).sum())
+    rhs = float((x.astype(np.float64) * back).sum())
+    assert lhs == rhs
+    # and the combine really touched something
+    assert np.abs(back).sum() > 0
+
+
+@pytest.mark.parametrize("de", [True, False])
+@pytest.mark.parametrize("dup", [False, True])
+def test_weight_reduction_is_the_adjoint_of_weight_dispatch(de, dup):
+    """For gradients shaped like the dispatched weights (zero where dispatch
+    writes 0), <dispatch_w(w), g> == <w, combine_topk_weights(g)>; and the
+    round trip combine_topk_weights(dispatch_w(w)) returns w on valid slots."""
+    rng = np.random.default_rng(53 + de + 2 * dup)
+    T, K, E, R = 60, 5, 12, 4
+    idx = _routing(rng, T, K, E, dup)
+    lay = O.layout(idx, E, R, 15, 4, de, True)
+    w = rng.integers(1, 8, (T, K)).astype(np.float32)
+    d = O.dispatch(lay, O.f32_to_bf16_bits(np.zeros((T, 16))), w)
+    rw = d["recv_topk_weights"]
+    g = rng.integers(-3, 4, rw.shape).astype(np.float32)
+    if de:
+        g[d["padding"]] = 0
+        g[~d["meta_defined"]] = 0
+    else:
+        g[d["recv_topk_idx"] < 0] = 0
+    back = O.combine_topk_weights(lay, g)
+    assert float((rw.astype(np.float64) * g).sum()) == float((w.astype(np.float64) * back).sum())
+    rt = O.combine_topk_weights(lay, rw)
+    assert np.array_equal(rt, np.where(lay["dst_buffer_slot_idx"] >= 0, w, 0))
+
+
+def test_weight_reduction_sums_every_column_of_a_tokens_rows():
+    idx = np.array([[0, 2, 3], [1, -1, 1], [-1, -1, -1]])   # E=4, R=2, L=2
+    lay = O.layout(idx, 4, 2, 2, 1, False, True)
+    d = lay["dst_buffer_slot_idx"]
+    rows = lay["rows_alloc"]
+    g = np.arange(rows * 3, dtype=np.float32).reshape(rows, 3) + 1
+    out = O.combine_topk_weights(lay, g)
+    r0, r1 = d[0, 0], d[0, 1]                     # token 0 on ranks 0 and 1
+    assert r0 != r1 and d[0, 2] == r1
+    assert np.array_equal(out[0], g[r0] + g[r1])
+    assert d[1, 0] == d[1, 2] and np.array_equal(out[1], g[d[1, 0]])   # one shared row
+    assert np.array_equal(out[2], np.zeros(3))                          # no rows
+    # expanded layout: each slot reads its own row
+    lay_e = O.layout(idx, 4, 2, 2, 1, True, True)
+    de = lay_e["dst_buffer_slot_idx"]
+    ge = np.arange(lay_e["rows_alloc"], dtype=np.float32) + 1
+    oe = O.combine_topk_weights(lay_e, ge)
+    assert np.array_equal(oe, np.where(de >= 0, ge[np.maximum(de, 0)], 0))

@@ -74,6 +74,29 @@ def stage_bytes(wl: W.Workload, T: int, topk_idx, rows_valid: int, rows_padding:
     return {"layout": layout, "dispatch": dispatch, "combine": combine}
 
 
+def backward_bytes(wl: W.Workload, T: int, topk_idx, rows_valid: int, rows_padding: int,
+                   rows_distinct_read: int) -> dict:
+    """Bytes of the backward pair for one batch.
+
+    combine_backward  : BF16 dispatch of the gradient without weights: each
+                        active source row read once (2H), per slot dst + idx
+                        reads (8 B), each destination row written (2H), padding
+                        rows zeroed (2H, with zero padding).
+    dispatch_backward : unweighted combine (each distinct row read once, 2H;
+                        dst 4 B/slot; output 2H per token) plus the weight
+                        reduction (dst 4 B/slot, the row's weight gradient,
+                        4 B expanded or 4K B rank layout, result 4 B/slot).
+    """
+    K, H = wl.num_topk, wl.hidden
+    t_active = int((topk_idx >= 0).any(dim=1).sum())
+    comb_b = (t_active * H * 2 + T * K * 8 + rows_valid * H * 2
+              + (rows_padding * H * 2 if wl.do_expand and wl.do_zero_padding else 0))
+    g_row = 4 if wl.do_expand else 4 * K
+    disp_b = (rows_distinct_read * H * 2 + T * K * 4 + T * H * 2
+              + T * K * 8 + rows_valid * g_row)
+    return {"combine_backward": comb_b, "dispatch_backward": disp_b}
+
+
 # ---------------------------------------------------------------------------
 # Clock sampling during the timed region
 # ---------------------------------------------------------------------------
@@ -313,6 +336,7 @@ def run_gpu(args, ws, rank, local):
     by = stage_bytes(wl, T, idx_h, valid_rows, pad_rows, distinct,
                      expert_bias=eb is not None)
     out_comb = torch.empty((T, H), dtype=torch.bfloat16, device=dev)
+    grad_recv_w = out0["recv_topk_weights"].clone()
     h0.free()
     del out0
 
@@ -413,6 +437,42 @@ def run_gpu(args, ws, rank, local):
     e2e_ms = max_over_ranks(e_s.elapsed_time(e_e) / e2e_steps, ws, dev)
     barrier(ws)
 
+    # Backward pair on one handle (layout untimed): combine_backward dispatches
+    # a [T, H] gradient, dispatch_backward combines a [rows, H] gradient and
+    # reduces the weight gradients.  L2 is flushed before each timed call.
+    bwd_by = backward_bytes(wl, T, idx_h, valid_rows, pad_rows, distinct)
+    hb = ep.ep_layout(cfg, idx)
+    g_recv = torch.empty((hb.rows_alloc, H), dtype=torch.bfloat16, device=dev)
+    g_x = torch.empty((T, H), dtype=torch.bfloat16, device=dev)
+    g_w = torch.empty((T, wl.num_topk), dtype=torch.float32, device=dev)
+
+    def bwd_step(ev=None):
+        flush_l2()
+        if ev:
+            ev[0].record(stream)
+        ep.ep_combine_backward(hb, x, g_recv)
+        if ev:
+            ev[1].record(stream)
+        flush_l2()
+        if ev:
+            ev[2].record(stream)
+        ep.ep_dispatch_backward(hb, y, grad_recv_w, g_x, g_w)
+        if ev:
+            ev[3].record(stream)
+
+    for _ in range(args.warmup):
+        bwd_step()
+    bwd_steps = max(8, args.steps // 4)
+    bev = [[torch.cuda.Event(enable_timing=True) for _ in range(4)] for _ in range(bwd_steps)]
+    torch.cuda.synchronize()
+    for i in range(bwd_steps):
+        bwd_step(bev[i])
+    torch.cuda.synchronize()
+    cb_ms = statistics.mean(e[0].elapsed_time(e[1]) for e in bev)
+    db_ms = statistics.mean(e[2].elapsed_time(e[3]) for e in bev)
+    hb.free()
+    del g_recv, g_x, g_w
+
     peaks = load_peaks()
     d_ms, c_ms = statistics.mean(dis_ms), statistics.mean(com_ms)
     dom = "combine" if c_ms >= d_ms else "dispatch"
@@ -457,6 +517,18 @@ def run_gpu(args, ws, rank, local):
                 "d2h_bytes_per_step": T * H * 2},
         "gpu_launches": launches,
         "clocks": clk,
+        "backward": {
+            "steps": bwd_steps,
+            "combine_backward": {"ms": round(cb_ms, 5), "bytes": bwd_by["combine_backward"],
+                                 "gbs": round(bwd_by["combine_backward"] / cb_ms / 1e6, 1),
+                                 "frac_of_peak": round(bwd_by["combine_backward"] / cb_ms / 1e6
+                                                       / peaks["hbm_gbs"], 4)},
+            "dispatch_backward": {"ms": round(db_ms, 5), "bytes": bwd_by["dispatch_backward"],
+                                  "gbs": round(bwd_by["dispatch_backward"] / db_ms / 1e6, 1),
+                                  "frac_of_peak": round(bwd_by["dispatch_backward"] / db_ms / 1e6
+                                                        / peaks["hbm_gbs"], 4)},
+            "gpu_launches": bwd_steps * ((1 if T > 0 else 0) + (2 if T > 0 else 0)),
+        },
     }
     if rank == 0 and ws == 1 and not args.no_cpu_baseline:
         cb = time_oracle(wl, args.cpu_sample_tokens, args.cpu_budget_s, seed=args.seed)

@@ -106,6 +106,10 @@ def load_library(path: str = LIB_PATH) -> ctypes.CDLL:
     lib.ep_dispatch.restype = ctypes.c_int
     lib.ep_combine.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp]
     lib.ep_combine.restype = ctypes.c_int
+    lib.ep_dispatch_backward.argtypes = [vp, vp, vp, vp, vp, vp]
+    lib.ep_dispatch_backward.restype = ctypes.c_int
+    lib.ep_combine_backward.argtypes = [vp, vp, vp, vp]
+    lib.ep_combine_backward.restype = ctypes.c_int
     lib.ep_handle_free.argtypes = [vp]
     lib.ep_handle_free.restype = None
     lib.ep_status_string.argtypes = [ctypes.c_int]
@@ -334,6 +338,48 @@ def ep_combine(handle: Handle, y: torch.Tensor, topk_weights: Optional[torch.Ten
     if st != EP_OK:
         raise EpError(st, "ep_combine")
     return out
+
+
+def ep_dispatch_backward(handle: Handle, grad_recv_x: torch.Tensor,
+                         grad_recv_topk_weights: Optional[torch.Tensor] = None,
+                         grad_x: Optional[torch.Tensor] = None,
+                         grad_topk_weights: Optional[torch.Tensor] = None, stream=None):
+    """Backward of dispatch: returns (grad_x [T, H] BF16, grad_topk_weights
+    [T, K] fp32 or None)."""
+    lib = load_library()
+    if grad_recv_x.dtype != torch.bfloat16:
+        raise ValueError(f"grad_recv_x must be bfloat16, got {grad_recv_x.dtype}")
+    dev = grad_recv_x.device
+    if grad_x is None:
+        grad_x = torch.empty((handle.T, handle.H), dtype=torch.bfloat16, device=dev)
+    if grad_recv_topk_weights is not None and grad_topk_weights is None:
+        grad_topk_weights = torch.empty((handle.T, handle.K), dtype=torch.float32, device=dev)
+    st = lib.ep_dispatch_backward(
+        ctypes.c_void_p(handle.ptr), _ptr(grad_recv_x, "grad_recv_x", torch.bfloat16),
+        _ptr(grad_recv_topk_weights, "grad_recv_topk_weights", torch.float32),
+        _ptr(grad_x, "grad_x", torch.bfloat16),
+        _ptr(grad_topk_weights, "grad_topk_weights", torch.float32), _stream_ptr(stream))
+    if st != EP_OK:
+        raise EpError(st, "ep_dispatch_backward")
+    return grad_x, grad_topk_weights
+
+
+def ep_combine_backward(handle: Handle, grad_combined_x: torch.Tensor,
+                        grad_recv_x: Optional[torch.Tensor] = None, stream=None) -> torch.Tensor:
+    """Backward of an unweighted combine: the BF16 gradient dispatched along
+    the handle, [rows_alloc, H]."""
+    lib = load_library()
+    if tuple(grad_combined_x.shape) != (handle.T, handle.H):
+        raise ValueError(f"grad shape {tuple(grad_combined_x.shape)} != ({handle.T}, {handle.H})")
+    if grad_recv_x is None:
+        grad_recv_x = torch.empty((handle.rows_alloc, handle.H), dtype=torch.bfloat16,
+                                  device=grad_combined_x.device)
+    st = lib.ep_combine_backward(
+        ctypes.c_void_p(handle.ptr), _ptr(grad_combined_x, "grad_combined_x", torch.bfloat16),
+        _ptr(grad_recv_x, "grad_recv_x", torch.bfloat16), _stream_ptr(stream))
+    if st != EP_OK:
+        raise EpError(st, "ep_combine_backward")
+    return grad_recv_x
 
 
 def ep_handle_free(handle: Handle) -> None:

@@ -135,6 +135,73 @@ ep_status cuda_status(cudaError_t e) {
 using ep::align_up;
 using ep::aligned;
 
+namespace ep {
+namespace {
+
+ep_status check_device(const ep_handle *h) {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return EP_ERR_CUDA;
+  return dev == h->device ? EP_OK : EP_ERR_INVALID_ARG;
+}
+
+DispatchParams dispatch_params(const ep_handle *h, const void *x, const float *topk_weights,
+                               void *recv_x, float *recv_sf, float *recv_topk_weights,
+                               int32_t *recv_topk_idx) {
+  const ep_config &c = h->cfg;
+  DispatchParams p{};
+  p.x = static_cast<const uint16_t *>(x);
+  p.topk_w = topk_weights;
+  p.topk32 = h->lp.topk32;
+  p.dst = h->lp.dst;
+  p.psum_e = h->lp.psum_e;
+  p.cnt_e = h->lp.cnt_e;
+  p.psum_pad = h->lp.psum_pad;
+  p.T = c.num_tokens;
+  p.K = c.num_topk;
+  p.E = c.num_experts;
+  p.L = c.num_experts / c.num_ranks;
+  p.H = c.hidden;
+  p.do_expand = c.do_expand;
+  p.zero_padding = c.do_expand && c.do_zero_padding;
+  p.max_pad_items = c.do_expand ? ((int64_t)c.num_experts * (c.expert_alignment - 1) + 7) / 8 : 0;
+  p.rows_alloc = h->rows_alloc;
+  p.sf_hidden_stride = h->sf_hidden_stride;
+  p.sf_token_stride = h->sf_token_stride;
+  p.recv_x = recv_x;
+  p.recv_sf = recv_sf;
+  p.recv_w = recv_topk_weights;
+  p.recv_idx = recv_topk_idx;
+  p.err = reinterpret_cast<unsigned *>(h->lp.ctrl + kCtrlError);
+  p.tok_scale = h->tok_scale;
+  p.meta = h->lp.meta;
+  p.num_rows = h->lp.ctrl + (c.do_expand ? kCtrlNumExpanded : kCtrlNumRecv);
+  return p;
+}
+
+CombineParams combine_params(const ep_handle *h, const void *y, const float *topk_weights,
+                             const void *bias_0, const void *bias_1, const void *expert_bias,
+                             void *out) {
+  const ep_config &c = h->cfg;
+  CombineParams p{};
+  p.y = static_cast<const uint16_t *>(y);
+  p.topk_w = topk_weights;
+  p.topk32 = h->lp.topk32;
+  p.dst = h->lp.dst;
+  p.bias0 = static_cast<const uint16_t *>(bias_0);
+  p.bias1 = static_cast<const uint16_t *>(bias_1);
+  p.ebias = static_cast<const uint16_t *>(expert_bias);
+  p.out = static_cast<uint16_t *>(out);
+  p.err = reinterpret_cast<unsigned *>(h->lp.ctrl + kCtrlError);
+  p.T = c.num_tokens;
+  p.K = c.num_topk;
+  p.H = c.hidden;
+  p.rows_alloc = h->rows_alloc;
+  return p;
+}
+
+}  // namespace
+}  // namespace ep
+
 extern "C" {
 
 const char *ep_status_string(ep_status s) {
@@ -402,37 +469,9 @@ ep_status ep_dispatch(ep_handle *h, const void *x, const float *topk_weights, vo
   if (topk_weights != nullptr && !aligned(topk_weights, 4)) return EP_ERR_INVALID_ARG;
   if (recv_topk_idx != nullptr && (c.do_expand || !aligned(recv_topk_idx, 4)))
     return EP_ERR_INVALID_ARG;
-  int dev = 0;
-  if (cudaGetDevice(&dev) != cudaSuccess) return EP_ERR_CUDA;
-  if (dev != h->device) return EP_ERR_INVALID_ARG;
-
-  ep::DispatchParams p{};
-  p.x = static_cast<const uint16_t *>(x);
-  p.topk_w = topk_weights;
-  p.topk32 = h->lp.topk32;
-  p.dst = h->lp.dst;
-  p.psum_e = h->lp.psum_e;
-  p.cnt_e = h->lp.cnt_e;
-  p.psum_pad = h->lp.psum_pad;
-  p.T = T;
-  p.K = c.num_topk;
-  p.E = c.num_experts;
-  p.L = c.num_experts / c.num_ranks;
-  p.H = c.hidden;
-  p.do_expand = c.do_expand;
-  p.zero_padding = c.do_expand && c.do_zero_padding;
-  p.max_pad_items = c.do_expand ? ((int64_t)c.num_experts * (c.expert_alignment - 1) + 7) / 8 : 0;
-  p.rows_alloc = h->rows_alloc;
-  p.sf_hidden_stride = h->sf_hidden_stride;
-  p.sf_token_stride = h->sf_token_stride;
-  p.recv_x = recv_x;
-  p.recv_sf = recv_sf;
-  p.recv_w = recv_topk_weights;
-  p.recv_idx = recv_topk_idx;
-  p.err = reinterpret_cast<unsigned *>(h->lp.ctrl + ep::kCtrlError);
-  p.tok_scale = h->tok_scale;
-  p.meta = h->lp.meta;
-  p.num_rows = h->lp.ctrl + (c.do_expand ? ep::kCtrlNumExpanded : ep::kCtrlNumRecv);
+  if (const ep_status st = ep::check_device(h); st != EP_OK) return st;
+  const ep::DispatchParams p = ep::dispatch_params(h, x, topk_weights, recv_x, recv_sf,
+                                                   recv_topk_weights, recv_topk_idx);
   if (h->rows_alloc == 0) return EP_OK;  // nothing lands anywhere
   const cudaError_t ce =
       ep::launch_dispatch(p, c.use_fp8, c.use_tma_aligned_col_major_sf, c.num_sms,
@@ -452,24 +491,62 @@ ep_status ep_combine(const ep_handle *h, const void *y, const float *topk_weight
   if ((bias_0 != nullptr && !aligned(bias_0, 16)) || (bias_1 != nullptr && !aligned(bias_1, 16)) ||
       (expert_bias != nullptr && !aligned(expert_bias, 16)))
     return EP_ERR_INVALID_ARG;
-  int dev = 0;
-  if (cudaGetDevice(&dev) != cudaSuccess) return EP_ERR_CUDA;
-  if (dev != h->device) return EP_ERR_INVALID_ARG;
-  ep::CombineParams p{};
-  p.y = static_cast<const uint16_t *>(y);
-  p.topk_w = topk_weights;
-  p.topk32 = h->lp.topk32;
-  p.dst = h->lp.dst;
-  p.bias0 = static_cast<const uint16_t *>(bias_0);
-  p.bias1 = static_cast<const uint16_t *>(bias_1);
-  p.ebias = static_cast<const uint16_t *>(expert_bias);
-  p.out = static_cast<uint16_t *>(out);
-  p.err = reinterpret_cast<unsigned *>(h->lp.ctrl + ep::kCtrlError);
-  p.T = T;
-  p.K = c.num_topk;
-  p.H = c.hidden;
-  p.rows_alloc = h->rows_alloc;
+  if (const ep_status st = ep::check_device(h); st != EP_OK) return st;
+  const ep::CombineParams p =
+      ep::combine_params(h, y, topk_weights, bias_0, bias_1, expert_bias, out);
   const cudaError_t ce = ep::launch_combine(p, c.num_sms, reinterpret_cast<cudaStream_t>(stream));
+  return ep::cuda_status(ce);
+}
+
+ep_status ep_dispatch_backward(const ep_handle *h, const void *grad_recv_x,
+                               const float *grad_recv_topk_weights, void *grad_x,
+                               float *grad_topk_weights, ep_stream_t stream) {
+  if (h == nullptr) return EP_ERR_INVALID_ARG;
+  const ep_config &c = h->cfg;
+  const int T = c.num_tokens;
+  if (T > 0 && (grad_x == nullptr || !aligned(grad_x, 16))) return EP_ERR_INVALID_ARG;
+  if (h->rows_alloc > 0 && (grad_recv_x == nullptr || !aligned(grad_recv_x, 16)))
+    return EP_ERR_INVALID_ARG;
+  // grad_topk_weights asks for the weight reduction; its input may be absent
+  // only when no row exists to hold it (rows_alloc == 0: every result is 0)
+  if (grad_topk_weights == nullptr && grad_recv_topk_weights != nullptr) return EP_ERR_INVALID_ARG;
+  if (grad_topk_weights != nullptr &&
+      (!aligned(grad_topk_weights, 4) ||
+       (h->rows_alloc > 0 &&
+        (grad_recv_topk_weights == nullptr || !aligned(grad_recv_topk_weights, 4)))))
+    return EP_ERR_INVALID_ARG;
+  if (const ep_status st = ep::check_device(h); st != EP_OK) return st;
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  const ep::CombineParams p =
+      ep::combine_params(h, grad_recv_x, nullptr, nullptr, nullptr, nullptr, grad_x);
+  cudaError_t ce = ep::launch_combine(p, c.num_sms, s);
+  if (ce == cudaSuccess && grad_topk_weights != nullptr) {
+    ep::CombineWeightsParams q{};
+    q.dst = h->lp.dst;
+    q.g = grad_recv_topk_weights;
+    q.out = grad_topk_weights;
+    q.T = T;
+    q.K = c.num_topk;
+    q.do_expand = c.do_expand;
+    ce = ep::launch_combine_weights(q, s);
+  }
+  return ep::cuda_status(ce);
+}
+
+ep_status ep_combine_backward(ep_handle *h, const void *grad_combined_x, void *grad_recv_x,
+                              ep_stream_t stream) {
+  if (h == nullptr) return EP_ERR_INVALID_ARG;
+  const ep_config &c = h->cfg;
+  if (c.num_tokens > 0 && (grad_combined_x == nullptr || !aligned(grad_combined_x, 16)))
+    return EP_ERR_INVALID_ARG;
+  if (h->rows_alloc > 0 && (grad_recv_x == nullptr || !aligned(grad_recv_x, 16)))
+    return EP_ERR_INVALID_ARG;
+  if (const ep_status st = ep::check_device(h); st != EP_OK) return st;
+  const ep::DispatchParams p =
+      ep::dispatch_params(h, grad_combined_x, nullptr, grad_recv_x, nullptr, nullptr, nullptr);
+  if (h->rows_alloc == 0) return EP_OK;
+  // always the BF16 copy, whatever the forward dispatch quantised to
+  const cudaError_t ce = ep::launch_dispatch(p, 0, 0, c.num_sms, reinterpret_cast<cudaStream_t>(stream));
   return ep::cuda_status(ce);
 }
 

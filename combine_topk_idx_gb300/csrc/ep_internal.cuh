@@ -86,6 +86,14 @@ struct CombineParams {
   int64_t rows_alloc;
 };
 
+struct CombineWeightsParams {
+  const int32_t *dst;     // [T, K]
+  const float *g;         // [rows_alloc] (expanded) or [rows_alloc, K] (rank layout)
+  float *out;             // [T, K]
+  int T, K;
+  int do_expand;
+};
+
 // Launchers (return the first CUDA error, cudaSuccess otherwise).
 cudaError_t launch_layout(const LayoutParams &p, cudaStream_t s);
 size_t layout_assign_smem(const LayoutParams &p);
@@ -93,6 +101,7 @@ int layout_rank_warps(int nkey);
 cudaError_t launch_dispatch(const DispatchParams &p, int use_fp8, int col_major,
                             int sm_cap, cudaStream_t s);
 cudaError_t launch_combine(const CombineParams &p, int sm_cap, cudaStream_t s);
+cudaError_t launch_combine_weights(const CombineWeightsParams &p, cudaStream_t s);
 
 // Device facts, cached per device.
 int device_sm_count(int device);

@@ -14,7 +14,8 @@
  *   ep_combine   per-token weighted gather-reduce of the expert outputs back
  *                to source-token order, fp32 accumulation, BF16 result;
  *
- * plus ep_handle_free.  The arguments follow the dispatch / combine / handle
+ * plus the backward pair (ep_dispatch_backward, ep_combine_backward) and
+ * ep_handle_free.  The arguments follow the dispatch / combine / handle
  * contract described in "DeepEP V2 notes, ch. 7: how V2 dispatch builds
  * expert inputs" (§7.1 input contract, §7.2 layout metadata and allocation,
  * §7.3 copy epilogue, §7.5 handle reuse) and "DeepEP V2 notes, ch. 8:
@@ -194,6 +195,46 @@ EP_API ep_status ep_dispatch(ep_handle *h, const void *x, const float *topk_weig
 EP_API ep_status ep_combine(const ep_handle *h, const void *y, const float *topk_weights,
                      const void *bias_0, const void *bias_1, const void *expert_bias,
                      void *out, ep_stream_t stream);
+
+/* ---- backward pair (DeepEP README, "Interfaces and examples":
+ *      dispatch_backward, combine_backward) ------------------------------- */
+
+/*
+ * ep_dispatch_backward -- the backward of ep_dispatch is a combine along the
+ * same handle that also reduces the received weight gradients.
+ *
+ * grad_recv_x: device BF16 [rows_alloc, H] in the dispatch layout, 16-byte
+ *   aligned.  grad_x (out): device BF16 [T, H], 16-byte aligned, no overlap.
+ *   grad_x[t] = bf16_rne(fp32 sum of grad_recv_x over the token's distinct
+ *   rows in slot order) -- ep_combine with topk_weights == NULL and no bias.
+ * grad_recv_topk_weights: NULL, or device fp32 [rows_alloc] (expanded) /
+ *   [rows_alloc, K] (rank layout), shaped like ep_dispatch's recv_topk_weights.
+ * grad_topk_weights (out): NULL (then grad_recv_topk_weights must be NULL
+ *   too), or device fp32 [T, K]; grad_recv_topk_weights may then be NULL only
+ *   if rows_alloc == 0 (every result is 0).  Per token, the fp32 sum of its distinct rows'
+ *   entries in slot order: expanded, slot k reads its own row (0 without
+ *   one); rank layout, column c sums column c of the token's rows (every
+ *   column, 0 for a token without rows).
+ * Ordered after ep_layout of the handle; returns EP_ERR_INVALID_ARG for a
+ * missing or misaligned pointer before touching the GPU.
+ */
+EP_API ep_status ep_dispatch_backward(const ep_handle *h, const void *grad_recv_x,
+                                      const float *grad_recv_topk_weights, void *grad_x,
+                                      float *grad_topk_weights, ep_stream_t stream);
+
+/*
+ * ep_combine_backward -- the backward of an unweighted ep_combine is a
+ * dispatch of the gradient along the same handle.
+ *
+ * grad_combined_x: device BF16 [T, H], 16-byte aligned.
+ * grad_recv_x (out): device BF16 [rows_alloc, H], 16-byte aligned: each
+ *   destination row gets its token's gradient row, bit for bit.  Always a
+ *   BF16 copy, also when cfg->use_fp8 quantises the forward dispatch.
+ *   Padding rows (expanded) are zeroed when cfg->do_zero_padding, else left
+ *   as they are; rows past the real total are not written.
+ */
+EP_API ep_status ep_combine_backward(ep_handle *h, const void *grad_combined_x,
+                                     void *grad_recv_x, ep_stream_t stream);
 
 /*
  * ep_handle_free -- releases the handle's device memory, stream-ordered on

@@ -100,3 +100,23 @@ def test_reference_arm_runs_the_oracle():
                           "--workload", "tiny", "--steps", "1", "--warmup", "3"],
                          capture_output=True, text=True, env=env2, timeout=300)
     assert out.returncode == 0 and out.stdout.strip() == ""
+
+
+def test_backward_bytes_match_definition():
+    for name in ("tiny", "decode"):
+        wl = W.WORKLOADS[name]
+        idx, _ = W.make_routing(wl, seed=0)
+        lay = O.layout(idx.numpy(), wl.num_experts, wl.num_ranks, wl.num_max_tokens_per_rank,
+                       wl.expert_alignment, wl.do_expand, True)
+        T, K, H = wl.num_tokens, wl.num_topk, wl.hidden
+        valid = (idx >= 0).numpy()
+        dst = lay["dst_buffer_slot_idx"]
+        distinct = int(np.unique(dst[dst >= 0]).size)
+        pad = int((lay["cnt_expert_aligned"] - lay["cnt_expert"]).sum()) if wl.do_expand else 0
+        rows = distinct
+        by = bench.backward_bytes(wl, T, idx, rows, pad, distinct)
+        act = int(valid.any(axis=1).sum())
+        zp = wl.do_expand and wl.do_zero_padding
+        assert by["combine_backward"] == act * H * 2 + T * K * 8 + rows * 2 * H + (pad * 2 * H if zp else 0)
+        g = 4 if wl.do_expand else 4 * K
+        assert by["dispatch_backward"] == distinct * 2 * H + T * K * 12 + T * H * 2 + rows * g

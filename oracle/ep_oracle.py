@@ -44,7 +44,7 @@ import numpy as np
 __all__ = [
     "align", "upper_bound_rows", "layout", "bf16_bits_to_f32", "f32_to_bf16_bits",
     "e4m3_encode", "e4m3_decode", "quantize_row", "dispatch", "combine",
-    "sf_numel", "sf_index", "FP8_BLOCK", "E4M3_MAX", "combine_topk_weights",
+    "sf_numel", "sf_index", "FP8_BLOCK", "E4M3_MAX", "combine_topk_weights", "dispatch_prequantised",
 ]
 
 FP8_BLOCK = 128        # 1x128 per-row scale blocks
@@ -329,8 +329,32 @@ def dispatch(lay, x_bits, topk_weights=None, use_fp8=False, col_major_sf=False,
       0 and -1 for its other slots.
     """
     x_bits = np.asarray(x_bits, dtype=np.uint16)
+    if use_fp8:
+        q, s = quantize_row(x_bits)
+        return _scatter_rows(lay, q, s, topk_weights, col_major_sf, do_zero_padding)
+    return _scatter_rows(lay, x_bits, None, topk_weights, False, do_zero_padding)
+
+
+def dispatch_prequantised(lay, x_fp8, x_sf, topk_weights=None, col_major_sf=False,
+                          do_zero_padding=False):
+    """Dispatch of an input that is already FP8: ``x = (e4m3 bytes [T, H],
+    fp32 scales [T, H/128])`` ("DeepEP V2 notes, ch. 7" §7.1 input contract,
+    §7.3 copy epilogue).  Nothing is quantised: each destination row gets its
+    token's bytes unchanged and its token's scales, written in the scale
+    layout the handle asks for (row-major, or TMA-aligned column-major).
+    Same outputs and masks as ``dispatch`` with ``use_fp8``."""
+    q = np.asarray(x_fp8, dtype=np.uint8)
+    s = np.asarray(x_sf, dtype=np.float32)
+    assert q.ndim == 2 and s.shape == (q.shape[0], q.shape[1] // FP8_BLOCK)
+    return _scatter_rows(lay, q, s, topk_weights, col_major_sf, do_zero_padding)
+
+
+def _scatter_rows(lay, payload, scales, topk_weights, col_major_sf, do_zero_padding):
+    """Copy each token's payload row (and scales) to its distinct rows, with
+    the per-row weights and local expert ids; see ``dispatch``."""
     T, K, E, R, L = lay["T"], lay["K"], lay["E"], lay["R"], lay["L"]
-    H = x_bits.shape[1]
+    H = payload.shape[1]
+    use_fp8 = scales is not None
     rows_alloc = lay["rows_alloc"]
     total = min(lay["total_rows"], rows_alloc)
     idx = lay["topk_idx"]
@@ -349,7 +373,6 @@ def dispatch(lay, x_bits, topk_weights=None, use_fp8=False, col_major_sf=False,
             payload_defined &= ~padding
 
     if use_fp8:
-        q, s = quantize_row(x_bits)
         recv_x = np.zeros((rows, H), dtype=np.uint8)
         recv_sf = np.zeros(sf_numel(rows, H, col_major_sf), dtype=np.float32)
     else:
@@ -371,12 +394,10 @@ def dispatch(lay, x_bits, topk_weights=None, use_fp8=False, col_major_sf=False,
             if row < 0 or row in done:
                 continue
             done.add(row)
+            recv_x[row] = payload[t]
             if use_fp8:
-                recv_x[row] = q[t]
                 for j in range(nb):
-                    recv_sf[sf_index(row, j, rows, H, col_major_sf)] = s[t, j]
-            else:
-                recv_x[row] = x_bits[t]
+                    recv_sf[sf_index(row, j, rows, H, col_major_sf)] = scales[t, j]
             if lay["do_expand"]:
                 if topk_weights is not None:
                     recv_w[row] = topk_weights[t, k]

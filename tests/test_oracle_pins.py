@@ -668,3 +668,54 @@ def test_weight_reduction_sums_every_column_of_a_tokens_rows():
     ge = np.arange(lay_e["rows_alloc"], dtype=np.float32) + 1
     oe = O.combine_topk_weights(lay_e, ge)
     assert np.array_equal(oe, np.where(de >= 0, ge[np.maximum(de, 0)], 0))
+
+
+# ---------------------------------------------------------------------------
+# Pre-quantised FP8 input (x given as e4m3 bytes + fp32 scales)
+# ---------------------------------------------------------------------------
+@pytest.mark.parametrize("de", [True, False])
+@pytest.mark.parametrize("cm", [True, False])
+def test_prequantised_dispatch_equals_quantising_dispatch(de, cm):
+    """Handing dispatch the bytes and scales that quantisation would produce
+    gives exactly the outputs of the quantising dispatch."""
+    rng = np.random.default_rng(61 + de + 2 * cm)
+    T, K, E, R, H = 90, 4, 16, 4, 256
+    idx = _routing(rng, T, K, E, dup=not de)
+    lay = O.layout(idx, E, R, 23, 8, de, True)
+    xb = _bf16(rng.normal(0, 1, (T, H)))
+    w = rng.random((T, K)).astype(np.float32)
+    q, sc = O.quantize_row(xb)
+    a = O.dispatch(lay, xb, w, True, cm, True)
+    b = O.dispatch_prequantised(lay, q, sc, w, cm, True)
+    for key in ("recv_x", "recv_sf", "recv_topk_weights", "payload_defined", "padding"):
+        assert np.array_equal(a[key], b[key]), key
+    if not de:
+        assert np.array_equal(a["recv_topk_idx"], b["recv_topk_idx"])
+
+
+@pytest.mark.parametrize("cm", [True, False])
+def test_prequantised_dispatch_copies_any_bytes_through_the_metadata(cm):
+    """Every byte value (NaN codes included) and every scale is copied
+    unchanged: row r holds the bytes and scales of token meta[r, 0]."""
+    rng = np.random.default_rng(67 + cm)
+    T, K, E, R, H = 64, 3, 8, 2, 384
+    idx = _routing(rng, T, K, E, dup=False)
+    lay = O.layout(idx, E, R, 32, 4, True, True)
+    q = rng.integers(0, 256, (T, H), dtype=np.uint8)
+    q[0, :] = np.arange(256).repeat(2)[:H].astype(np.uint8)
+    sc = rng.standard_normal((T, H // 128)).astype(np.float32)
+    sc[1, 0] = np.float32(-0.0)
+    d = O.dispatch_prequantised(lay, q, sc, None, cm, True)
+    meta = lay["recv_src_metadata"]
+    rows = lay["rows_alloc"]
+    nb = H // 128
+    for r in range(rows):
+        tok = int(meta[r, 0])
+        for j in range(nb):
+            got = d["recv_sf"][O.sf_index(r, j, rows, H, cm)]
+            want = sc[tok, j] if tok >= 0 else np.float32(0)
+            assert got.tobytes() == np.float32(want).tobytes()
+        if tok >= 0:
+            assert np.array_equal(d["recv_x"][r], q[tok])
+        else:
+            assert not d["recv_x"][r].any()

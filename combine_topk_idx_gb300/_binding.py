@@ -106,6 +106,8 @@ def load_library(path: str = LIB_PATH) -> ctypes.CDLL:
     lib.ep_dispatch.restype = ctypes.c_int
     lib.ep_combine.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp]
     lib.ep_combine.restype = ctypes.c_int
+    lib.ep_dispatch_fp8.argtypes = [vp, vp, vp, i64, i64, vp, vp, vp, vp, vp, vp]
+    lib.ep_dispatch_fp8.restype = ctypes.c_int
     lib.ep_dispatch_backward.argtypes = [vp, vp, vp, vp, vp, vp]
     lib.ep_dispatch_backward.restype = ctypes.c_int
     lib.ep_combine_backward.argtypes = [vp, vp, vp, vp]
@@ -319,6 +321,33 @@ def ep_dispatch(handle: Handle, x: torch.Tensor, topk_weights: Optional[torch.Te
         _ptr(recv_topk_idx, "recv_topk_idx", torch.int32), _stream_ptr(stream))
     if st != EP_OK:
         raise EpError(st, "ep_dispatch")
+
+
+def ep_dispatch_fp8(handle: Handle, x_fp8: torch.Tensor, x_sf: torch.Tensor,
+                    topk_weights: Optional[torch.Tensor], recv_x: torch.Tensor,
+                    recv_sf: torch.Tensor, recv_topk_weights: Optional[torch.Tensor] = None,
+                    recv_topk_idx: Optional[torch.Tensor] = None, stream=None) -> None:
+    """Dispatch of a pre-quantised input: ``x_fp8`` e4m3 [T, H] (uint8 or
+    float8_e4m3fn) and ``x_sf`` fp32 [T, H/128] with any non-negative strides
+    (row-major, or a column-major view), copied without re-quantisation."""
+    lib = load_library()
+    if tuple(x_fp8.shape) != (handle.T, handle.H):
+        raise ValueError(f"x_fp8 shape {tuple(x_fp8.shape)} != ({handle.T}, {handle.H})")
+    if tuple(x_sf.shape) != (handle.T, handle.H // 128):
+        raise ValueError(f"x_sf shape {tuple(x_sf.shape)} != ({handle.T}, {handle.H // 128})")
+    if not x_sf.is_cuda or x_sf.dtype != torch.float32:
+        raise ValueError("x_sf must be a CUDA float32 tensor")
+    ts, hs = x_sf.stride()
+    st = lib.ep_dispatch_fp8(
+        ctypes.c_void_p(handle.ptr), _ptr(x_fp8, "x_fp8", (torch.uint8, torch.float8_e4m3fn)),
+        x_sf.data_ptr() if x_sf.numel() > 0 else None, ts, hs,
+        _ptr(topk_weights, "topk_weights", torch.float32),
+        _ptr(recv_x, "recv_x", (torch.uint8, torch.float8_e4m3fn)),
+        _ptr(recv_sf, "recv_sf", torch.float32),
+        _ptr(recv_topk_weights, "recv_topk_weights", torch.float32),
+        _ptr(recv_topk_idx, "recv_topk_idx", torch.int32), _stream_ptr(stream))
+    if st != EP_OK:
+        raise EpError(st, "ep_dispatch_fp8")
 
 
 def ep_combine(handle: Handle, y: torch.Tensor, topk_weights: Optional[torch.Tensor] = None,

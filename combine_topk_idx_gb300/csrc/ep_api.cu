@@ -175,6 +175,9 @@ DispatchParams dispatch_params(const ep_handle *h, const void *x, const float *t
   p.tok_scale = h->tok_scale;
   p.meta = h->lp.meta;
   p.num_rows = h->lp.ctrl + (c.do_expand ? kCtrlNumExpanded : kCtrlNumRecv);
+  p.sf_src = h->tok_scale;
+  p.sf_src_ts = c.hidden / 128;
+  p.sf_src_hs = 1;
   return p;
 }
 
@@ -476,6 +479,43 @@ ep_status ep_dispatch(ep_handle *h, const void *x, const float *topk_weights, vo
   const cudaError_t ce =
       ep::launch_dispatch(p, c.use_fp8, c.use_tma_aligned_col_major_sf, c.num_sms,
                           reinterpret_cast<cudaStream_t>(stream));
+  return ep::cuda_status(ce);
+}
+
+ep_status ep_dispatch_fp8(ep_handle *h, const void *x_fp8, const float *x_sf,
+                          int64_t x_sf_token_stride, int64_t x_sf_hidden_stride,
+                          const float *topk_weights, void *recv_x, float *recv_sf,
+                          float *recv_topk_weights, int32_t *recv_topk_idx, ep_stream_t stream) {
+  if (h == nullptr) return EP_ERR_INVALID_ARG;
+  const ep_config &c = h->cfg;
+  if (!c.use_fp8) return EP_ERR_INVALID_ARG;  // the handle's receive layout must be FP8
+  const int T = c.num_tokens;
+  if (T > 0 && (x_fp8 == nullptr || !aligned(x_fp8, 16) || x_sf == nullptr || !aligned(x_sf, 4)))
+    return EP_ERR_INVALID_ARG;
+  if (x_sf_token_stride < 0 || x_sf_hidden_stride < 0) return EP_ERR_INVALID_ARG;
+  if (x_sf_token_stride > (int64_t(1) << 40) || x_sf_hidden_stride > (int64_t(1) << 40))
+    return EP_ERR_INVALID_ARG;
+  if (h->rows_alloc > 0 && (recv_x == nullptr || !aligned(recv_x, 16) || recv_sf == nullptr ||
+                            !aligned(recv_sf, 4)))
+    return EP_ERR_INVALID_ARG;
+  if (recv_topk_weights != nullptr && (topk_weights == nullptr || !aligned(recv_topk_weights, 4)))
+    return EP_ERR_INVALID_ARG;
+  if (topk_weights != nullptr && !aligned(topk_weights, 4)) return EP_ERR_INVALID_ARG;
+  if (recv_topk_idx != nullptr && (c.do_expand || !aligned(recv_topk_idx, 4)))
+    return EP_ERR_INVALID_ARG;
+  if (const ep_status st = ep::check_device(h); st != EP_OK) return st;
+  ep::DispatchParams p = ep::dispatch_params(h, nullptr, topk_weights, recv_x, recv_sf,
+                                             recv_topk_weights, recv_topk_idx);
+  p.xq = static_cast<const uint8_t *>(x_fp8);
+  p.xs = x_sf;
+  p.xs_ts = x_sf_token_stride;
+  p.xs_hs = x_sf_hidden_stride;
+  p.sf_src = x_sf;
+  p.sf_src_ts = x_sf_token_stride;
+  p.sf_src_hs = x_sf_hidden_stride;
+  if (h->rows_alloc == 0) return EP_OK;
+  const cudaError_t ce = ep::launch_dispatch(p, 2, c.use_tma_aligned_col_major_sf, c.num_sms,
+                                             reinterpret_cast<cudaStream_t>(stream));
   return ep::cuda_status(ce);
 }
 

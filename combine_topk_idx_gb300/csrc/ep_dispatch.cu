@@ -17,7 +17,11 @@
 //           packed cvt.rn.satfinite.e4m3x2 -- into an output stage, then one
 //           thread issues one cp.async.bulk shared->global store per distinct
 //           destination row while the others write the scales;
-//     BF16: one thread stores the input stage itself to every row.
+//     BF16: one thread stores the input stage itself to every row;
+//     pre-quantised FP8 input (x given as e4m3 bytes + fp32 scales, §7.1):
+//           the same copy of the H-byte row, while the other threads copy
+//           the token's scales to each row (row-major) or leave them to the
+//           column-major gather, which then reads the caller's scales.
 // The source row is read from HBM once and quantised once whatever K is; the
 // TMA engine moves every payload byte.  After the tokens, the consumer warps
 // zero the alignment padding rows in 8-row work items.  Every mbarrier wait
@@ -36,6 +40,11 @@ constexpr int kMaxConsumers = 224;
 constexpr int kWaitIters = 4000;          // x kWaitHintNs: gives up after ~2 s
 constexpr uint32_t kWaitHintNs = 500000;
 constexpr int kBarConsumers = 1;          // named barrier id (0 is __syncthreads)
+
+// What the kernel does with a source row.
+constexpr int kModeBf16 = 0;    // BF16 in, BF16 copy out
+constexpr int kModeQuant = 1;   // BF16 in, quantised to e4m3 + fp32 scales
+constexpr int kModePreq = 2;    // e4m3 + fp32 scales in, copied
 
 struct TokenMeta {
   int rows[EP_MAX_TOPK];
@@ -107,8 +116,10 @@ __device__ __forceinline__ Routing load_routing(const DispatchParams &p, int t, 
   return r;
 }
 
-template <bool FP8, bool COL_MAJOR>
+template <int MODE, bool COL_MAJOR>
 __global__ void __launch_bounds__(kMaxConsumers + 32, 1) dispatch_kernel(DispatchParams p) {
+  constexpr bool FP8 = MODE == kModeQuant;         // quantise in the consumers
+  constexpr bool FP8_OUT = MODE != kModeBf16;      // e4m3 payload + scales
   extern __shared__ __align__(128) uint8_t smem[];
   __shared__ __align__(8) uint64_t full[kStages];
   __shared__ __align__(8) uint64_t empty[kStages];
@@ -116,9 +127,9 @@ __global__ void __launch_bounds__(kMaxConsumers + 32, 1) dispatch_kernel(Dispatc
   __shared__ int prow_s[2][kPadRowsPerItem];
 
   const int H = p.H;
-  const int in_bytes = 2 * H;                              // BF16 source row
+  const int in_bytes = MODE == kModePreq ? H : 2 * H;     // source row
   const int in_stage = (in_bytes + 127) / 128 * 128;
-  const int out_bytes = FP8 ? H : 2 * H;                   // destination row
+  const int out_bytes = FP8_OUT ? H : 2 * H;               // destination row
   const int out_stage = FP8 ? (H + 127) / 128 * 128 : 0;
   const int nb = H / kFp8Block;
   const int nb_pad = (nb + 31) / 32 * 32;
@@ -193,8 +204,10 @@ __global__ void __launch_bounds__(kMaxConsumers + 32, 1) dispatch_kernel(Dispatc
       if (lane == 0) {
         if (n > 0) {
           mbar_arrive_expect_tx(&full[s], (uint32_t)in_bytes);
-          bulk_load_g2s_hint(in0 + s * in_stage, p.x + (int64_t)t * H, (uint32_t)in_bytes, &full[s],
-                             stream_pol);
+          const void *src = MODE == kModePreq
+                                ? static_cast<const void *>(p.xq + (int64_t)t * H)
+                                : static_cast<const void *>(p.x + (int64_t)t * H);
+          bulk_load_g2s_hint(in0 + s * in_stage, src, (uint32_t)in_bytes, &full[s], stream_pol);
         } else {
           mbar_arrive(&full[s]);
         }
@@ -215,7 +228,7 @@ __global__ void __launch_bounds__(kMaxConsumers + 32, 1) dispatch_kernel(Dispatc
   int pi = 0;
   for (int64_t item = blockIdx.x; item < num_items; item += gridDim.x) {
     if (item >= p.T) {  // every token item comes before the padding items
-      zero_padding_item(p, (int)(item - p.T), npad, prow_s[pi & 1], FP8, COL_MAJOR, ctid, nct);
+      zero_padding_item(p, (int)(item - p.T), npad, prow_s[pi & 1], FP8_OUT, COL_MAJOR, ctid, nct);
       ++pi;
       continue;
     }
@@ -295,14 +308,22 @@ __global__ void __launch_bounds__(kMaxConsumers + 32, 1) dispatch_kernel(Dispatc
       __syncwarp();
       if (lane == 0) mbar_arrive(&empty[s]);
     } else {
-      // BF16: the input stage is the payload; it is released once its bulk
-      // stores have read it.
+      // BF16 or pre-quantised: the input stage is the payload; it is released
+      // once its bulk stores have read it.
       if (ctid == 0) {
         for (int r = 0; r < n; ++r)
           bulk_store_s2g_hint(recv + (int64_t)meta[s].rows[r] * out_bytes, in, (uint32_t)out_bytes,
                               stream_pol);
         bulk_commit();
         bulk_wait_read<0>();
+      }
+      if constexpr (MODE == kModePreq && !COL_MAJOR) {
+        // row-major scales: the token's nb scales to each of its rows
+        for (int e = ctid; e < n * nb; e += nct) {
+          const int r = e / nb, j = e - r * nb;
+          p.recv_sf[(int64_t)meta[s].rows[r] * nb + j] =
+              __ldg(p.xs + (int64_t)t * p.xs_ts + (int64_t)j * p.xs_hs);
+        }
       }
       __syncwarp();
       if (lane == 0) mbar_arrive(&empty[s]);
@@ -313,7 +334,8 @@ __global__ void __launch_bounds__(kMaxConsumers + 32, 1) dispatch_kernel(Dispatc
 }
 
 // Column-major scale factors of every destination row, gathered from the
-// per-token scales through the row's source token (recv_src_metadata).  Grid
+// per-token scales (sf_src: the dispatch kernel's own, or the caller's for a
+// pre-quantised input) through the row's source token (recv_src_metadata).  Grid
 // (row blocks, groups of 4 scale blocks): thread (row, g) loads 16 bytes of
 // its token's scales and writes scale blocks 4g..4g+3 of its row, so for
 // each block the threads of a warp write 32 consecutive rows.  Padding rows
@@ -328,12 +350,12 @@ __global__ void __launch_bounds__(256) sf_expand_kernel(DispatchParams p) {
   const int tok = __ldg(&reinterpret_cast<const int2 *>(p.meta)[row].x);
   float v[4] = {0.f, 0.f, 0.f, 0.f};
   if (tok >= 0) {
-    const float *src = p.tok_scale + (int64_t)tok * nb + j0;
-    if ((nb & 3) == 0) {
+    const float *src = p.sf_src + (int64_t)tok * p.sf_src_ts + (int64_t)j0 * p.sf_src_hs;
+    if (p.sf_src_vec4) {
       const float4 q = __ldg(reinterpret_cast<const float4 *>(src));
       v[0] = q.x; v[1] = q.y; v[2] = q.z; v[3] = q.w;
     } else {
-      for (int u = 0; u < 4 && j0 + u < nb; ++u) v[u] = __ldg(src + u);
+      for (int u = 0; u < 4 && j0 + u < nb; ++u) v[u] = __ldg(src + (int64_t)u * p.sf_src_hs);
     }
   }
   float *dst = p.recv_sf + row + (int64_t)j0 * p.sf_hidden_stride;
@@ -342,16 +364,22 @@ __global__ void __launch_bounds__(256) sf_expand_kernel(DispatchParams p) {
     if (j0 + u < nb) dst[(int64_t)u * p.sf_hidden_stride] = v[u];
 }
 
-template <bool FP8, bool CM>
-cudaError_t launch_one(const DispatchParams &p, int sm_cap, cudaStream_t s) {
-  auto kern = dispatch_kernel<FP8, CM>;
+template <int MODE, bool CM>
+cudaError_t launch_one(const DispatchParams &p0, int sm_cap, cudaStream_t s) {
+  constexpr bool FP8 = MODE == kModeQuant;
+  auto kern = dispatch_kernel<MODE, CM>;
+  DispatchParams p = p0;
+  // the scale gather reads 4 scales of a token at once when they are
+  // contiguous and 16-byte aligned
+  p.sf_src_vec4 = (p.H / kFp8Block) % 4 == 0 && p.sf_src_hs == 1 && p.sf_src_ts % 4 == 0 &&
+                  reinterpret_cast<uintptr_t>(p.sf_src) % 16 == 0;
   const int H = p.H;
   const int nvec = H / 8;
   // FP8: consumer threads cover the row in whole 16-lane groups; BF16: the
   // consumers only issue bulk copies and zero padding rows.
   const int consumers = FP8 ? std::min(kMaxConsumers, (nvec + 31) / 32 * 32) : 64;
   const int threads = consumers + 32;
-  const size_t in_stage = (size_t)(2 * H + 127) / 128 * 128;
+  const size_t in_stage = (size_t)((MODE == kModePreq ? H : 2 * H) + 127) / 128 * 128;
   const size_t out_stage = FP8 ? (size_t)(H + 127) / 128 * 128 : 0;
   const size_t smem = kStages * (in_stage + out_stage) +
                       (FP8 && !CM ? kStages * sizeof(float) * ((H / kFp8Block + 31) / 32 * 32) : 0);
@@ -374,7 +402,7 @@ cudaError_t launch_one(const DispatchParams &p, int sm_cap, cudaStream_t s) {
   if (grid <= 0) return cudaSuccess;
   kern<<<(int)grid, threads, smem, s>>>(p);
   err = cudaGetLastError();
-  if (err != cudaSuccess || !FP8 || !CM) return err;
+  if (err != cudaSuccess || MODE == kModeBf16 || !CM) return err;
   // column-major scales: one gather pass (rows past the real total, in an
   // upper-bound allocation, are left untouched)
   const int64_t sf_grid = (p.rows_alloc + 255) / 256;
@@ -397,11 +425,15 @@ cudaError_t launch_one(const DispatchParams &p, int sm_cap, cudaStream_t s) {
 
 }  // namespace
 
-cudaError_t launch_dispatch(const DispatchParams &p, int use_fp8, int col_major, int sm_cap,
+cudaError_t launch_dispatch(const DispatchParams &p, int mode, int col_major, int sm_cap,
                             cudaStream_t s) {
-  if (use_fp8)
-    return col_major ? launch_one<true, true>(p, sm_cap, s) : launch_one<true, false>(p, sm_cap, s);
-  return launch_one<false, false>(p, sm_cap, s);
+  if (mode == kModeQuant)
+    return col_major ? launch_one<kModeQuant, true>(p, sm_cap, s)
+                     : launch_one<kModeQuant, false>(p, sm_cap, s);
+  if (mode == kModePreq)
+    return col_major ? launch_one<kModePreq, true>(p, sm_cap, s)
+                     : launch_one<kModePreq, false>(p, sm_cap, s);
+  return launch_one<kModeBf16, false>(p, sm_cap, s);
 }
 
 }  // namespace ep

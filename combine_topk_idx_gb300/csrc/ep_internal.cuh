@@ -71,6 +71,15 @@ struct DispatchParams {
   float *tok_scale;       // [T, H/128] FP8 scales per source token (handle scratch)
   const int32_t *meta;    // [rows, 2] recv_src_metadata
   const int32_t *num_rows;  // device total rows of the layout
+  // pre-quantised input: e4m3 bytes [T, H] and scales x_sf[t * xs_ts + j * xs_hs]
+  const uint8_t *xq;
+  const float *xs;
+  int64_t xs_ts, xs_hs;
+  // per-token scales read by the column-major scale gather (element (t, j) at
+  // sf_src[t * sf_src_ts + j * sf_src_hs]); sf_src_vec4 is set by the launcher
+  const float *sf_src;
+  int64_t sf_src_ts, sf_src_hs;
+  int sf_src_vec4;
 };
 
 struct CombineParams {
@@ -98,7 +107,8 @@ struct CombineWeightsParams {
 cudaError_t launch_layout(const LayoutParams &p, cudaStream_t s);
 size_t layout_assign_smem(const LayoutParams &p);
 int layout_rank_warps(int nkey);
-cudaError_t launch_dispatch(const DispatchParams &p, int use_fp8, int col_major,
+// mode: 0 BF16 copy, 1 quantise BF16 to e4m3 + scales, 2 copy a pre-quantised input
+cudaError_t launch_dispatch(const DispatchParams &p, int mode, int col_major,
                             int sm_cap, cudaStream_t s);
 cudaError_t launch_combine(const CombineParams &p, int sm_cap, cudaStream_t s);
 cudaError_t launch_combine_weights(const CombineWeightsParams &p, cudaStream_t s);

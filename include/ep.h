@@ -178,6 +178,26 @@ EP_API ep_status ep_dispatch(ep_handle *h, const void *x, const float *topk_weig
                       int32_t *recv_topk_idx, ep_stream_t stream);
 
 /*
+ * ep_dispatch_fp8 -- copy epilogue for an input that is already FP8 (§7.1:
+ * x may be an FP8 data + scale-factor tuple; §7.3 scale-factor layouts).
+ *
+ * Requires cfg->use_fp8 = 1 (the receive buffers are FP8); nothing is
+ * quantised.  x_fp8: device e4m3 bytes [T, H], 16-byte aligned.  x_sf: device
+ * fp32, the scale of token t and 128-element block j at
+ *   x_sf[t * x_sf_token_stride + j * x_sf_hidden_stride]   (strides >= 0),
+ * e.g. row-major [T, H/128] (H/128, 1) or column-major TMA-aligned
+ * (1, align(T, 4)).  Every destination row gets its token's bytes unchanged
+ * and its token's scales in the handle's layout (row-major, or column-major
+ * with use_tma_aligned_col_major_sf); padding rows, weights and local expert
+ * ids exactly as ep_dispatch.  The other arguments are those of ep_dispatch.
+ */
+EP_API ep_status ep_dispatch_fp8(ep_handle *h, const void *x_fp8, const float *x_sf,
+                                 int64_t x_sf_token_stride, int64_t x_sf_hidden_stride,
+                                 const float *topk_weights, void *recv_x, float *recv_sf,
+                                 float *recv_topk_weights, int32_t *recv_topk_idx,
+                                 ep_stream_t stream);
+
+/*
  * ep_combine -- reduce expert outputs back to token order (§8.1 combine
  * along the handle; vLLM PR #52781 review: combine requires BF16 input and
  * may be called with topk_weights = None).

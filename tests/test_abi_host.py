@@ -178,6 +178,7 @@ def test_entry_points_reject_bad_arguments_before_any_cuda_call(ep):
     lib.ep_handle_free(None)
     assert lib.ep_dispatch_backward(None, None, None, None, None, None) == 1
     assert lib.ep_combine_backward(None, None, None, None) == 1
+    assert lib.ep_dispatch_fp8(None, None, None, 0, 0, None, None, None, None, None, None) == 1
     # allocation-free layout: sync mode, missing buffers, oversized problems
     b = ep.EpLayoutBuffersC()
     fn = lib.ep_layout_noalloc

@@ -120,3 +120,19 @@ def test_backward_bytes_match_definition():
         assert by["combine_backward"] == act * H * 2 + T * K * 8 + rows * 2 * H + (pad * 2 * H if zp else 0)
         g = 4 if wl.do_expand else 4 * K
         assert by["dispatch_backward"] == distinct * 2 * H + T * K * 12 + T * H * 2 + rows * g
+
+
+def test_prequantised_bytes_match_definition():
+    wl = W.WORKLOADS["prefill"]
+    T = 256
+    idx, _ = W.make_routing(wl, seed=0, num_tokens=T)
+    lay = O.layout(idx.numpy(), wl.num_experts, wl.num_ranks, wl.num_max_tokens_per_rank,
+                   wl.expert_alignment, wl.do_expand, True)
+    valid = (idx >= 0).numpy()
+    rows = int(valid.sum())
+    pad = int((lay["cnt_expert_aligned"] - lay["cnt_expert"]).sum())
+    act = int(valid.any(axis=1).sum())
+    H, K = wl.hidden, wl.num_topk
+    sf = H // 128 * 4
+    assert bench.prequantised_bytes(wl, T, idx, rows, pad) == \
+        act * (H + sf) + T * K * 12 + rows * (H + sf + 4) + pad * (H + sf + 4)

@@ -45,6 +45,7 @@ __all__ = [
     "align", "upper_bound_rows", "layout", "bf16_bits_to_f32", "f32_to_bf16_bits",
     "e4m3_encode", "e4m3_decode", "quantize_row", "dispatch", "combine",
     "sf_numel", "sf_index", "FP8_BLOCK", "E4M3_MAX", "combine_topk_weights", "dispatch_prequantised",
+    "layout_fixed_capacity",
 ]
 
 FP8_BLOCK = 128        # 1x128 per-row scale blocks
@@ -83,18 +84,31 @@ def upper_bound_rows(num_tokens, num_topk, num_experts, num_ranks, M, A, do_expa
     return (per_rank, glob, rows) if parts else rows
 
 
-def sf_numel(rows_alloc, hidden, col_major):
-    """Number of fp32 scale slots the caller allocates for FP8 dispatch."""
+def sf_numel(rows_alloc, hidden, col_major, capacity=None):
+    """Number of fp32 scale slots the caller allocates for FP8 dispatch.
+
+    ``capacity``: the fixed-capacity layout (``layout_fixed_capacity``), whose
+    column-major scales are laid out per expert (reading R20)."""
     nb = hidden // FP8_BLOCK
+    if col_major and capacity is not None:
+        return (rows_alloc // capacity) * nb * int(align(capacity, 4))
     return nb * int(align(rows_alloc, 4)) if col_major else nb * rows_alloc
 
 
-def sf_index(row, j, rows_alloc, hidden, col_major):
+def sf_index(row, j, rows_alloc, hidden, col_major, capacity=None):
     """Flat index of scale block ``j`` of ``row``.
 
     Column-major TMA-aligned layout (§7.3): the hidden-block stride is the row
-    count rounded up to 4 fp32 (16 bytes) -- reading R10.
+    count rounded up to 4 fp32 (16 bytes) -- reading R10.  In the
+    fixed-capacity layout each expert's slab [capacity, H/128] is column-major
+    on its own, with the row stride 1 and the block stride
+    ``align(capacity, 4)`` (reading R20).  Row-major is ``row * H/128 + j``
+    in every layout.
     """
+    if col_major and capacity is not None:
+        cap_al = int(align(capacity, 4))
+        e, i = np.divmod(row, capacity)
+        return e * (hidden // FP8_BLOCK) * cap_al + j * cap_al + i
     if col_major:
         return row + j * int(align(rows_alloc, 4))
     return row * (hidden // FP8_BLOCK) + j
@@ -221,6 +235,52 @@ def layout(topk_idx, num_experts, num_ranks, num_max_tokens_per_rank,
         "total_rows": total_rows,
         "rows_alloc": rows_alloc,
     }
+
+
+def layout_fixed_capacity(topk_idx, num_experts, num_ranks, num_max_tokens_per_rank):
+    """Fixed-capacity per-expert layout of the low-latency kernels (DeepEP
+    README, "Interfaces and examples", low_latency_dispatch: per rank a
+    [num_local_experts, num_max_dispatch_tokens_per_rank * num_ranks, hidden]
+    receive tensor plus a per-expert count; CUDA-graph compatible).
+
+    Reading R20: one GPU holds all R ranks' tensors back to back, so the rows
+    form E slabs of ``capacity = M * R`` rows; expert e's i-th slot (slots in
+    ascending (t, k), reading R2) lands at row ``e * capacity + i``.  Rows
+    past a slab's count are unused (not written: unspecified).  No alignment
+    padding.  A slot whose position reaches the capacity (possible only when
+    a token repeats an expert) is dropped and raises the overflow error bit.
+    Counts, rank outputs and prefix sums are those of ``layout`` with A = 1;
+    ``rows_alloc = E * capacity`` whatever the counts are.
+    """
+    E, R, M = num_experts, num_ranks, num_max_tokens_per_rank
+    lay = layout(topk_idx, E, R, M, 1, True, True)
+    T, K = lay["T"], lay["K"]
+    cap = M * R
+    idx = lay["topk_idx"]
+    rows_alloc = E * cap
+    dst = np.full((T, K), -1, dtype=np.int64)
+    meta = np.full((rows_alloc, 2), -1, dtype=np.int64)
+    defined = np.zeros(rows_alloc, dtype=bool)
+    error = lay["error"]
+    flat_idx = idx.reshape(-1)
+    flat_dst = dst.reshape(-1)
+    for e in range(E):
+        slots = np.flatnonzero(flat_idx == e)              # ascending (t, k)
+        n = min(slots.size, cap)
+        if slots.size > cap:
+            error |= 2
+        rows = e * cap + np.arange(n)
+        flat_dst[slots[:n]] = rows
+        meta[rows, 0] = slots[:n] // K
+        meta[rows, 1] = slots[:n] % K
+        defined[rows] = True
+    lay = dict(lay)
+    lay.update({
+        "error": error, "dst_buffer_slot_idx": dst, "recv_src_metadata": meta,
+        "rows_alloc": rows_alloc, "capacity": cap, "fixed_capacity": True,
+        "row_defined": defined, "do_cpu_sync": False,
+    })
+    return lay
 
 
 # --------------------------------------------------------------------------
@@ -361,11 +421,15 @@ def _scatter_rows(lay, payload, scales, topk_weights, col_major_sf, do_zero_padd
     dst = lay["dst_buffer_slot_idx"]
     rows = rows_alloc
 
+    capacity = lay.get("capacity")
     payload_defined = np.zeros(rows, dtype=bool)
-    payload_defined[:total] = True
+    if capacity is not None:
+        payload_defined |= lay["row_defined"]
+    else:
+        payload_defined[:total] = True
     meta_defined = payload_defined.copy()
     padding = np.zeros(rows, dtype=bool)
-    if lay["do_expand"]:
+    if lay["do_expand"] and capacity is None:
         pe, ce = lay["psum_expert"], lay["cnt_expert"]
         for e in range(E):
             padding[min(pe[e] + ce[e], rows):min(pe[e + 1], rows)] = True
@@ -374,7 +438,7 @@ def _scatter_rows(lay, payload, scales, topk_weights, col_major_sf, do_zero_padd
 
     if use_fp8:
         recv_x = np.zeros((rows, H), dtype=np.uint8)
-        recv_sf = np.zeros(sf_numel(rows, H, col_major_sf), dtype=np.float32)
+        recv_sf = np.zeros(sf_numel(rows, H, col_major_sf, capacity), dtype=np.float32)
     else:
         recv_x = np.zeros((rows, H), dtype=np.uint16)
         recv_sf = None
@@ -397,7 +461,7 @@ def _scatter_rows(lay, payload, scales, topk_weights, col_major_sf, do_zero_padd
             recv_x[row] = payload[t]
             if use_fp8:
                 for j in range(nb):
-                    recv_sf[sf_index(row, j, rows, H, col_major_sf)] = scales[t, j]
+                    recv_sf[sf_index(row, j, rows, H, col_major_sf, capacity)] = scales[t, j]
             if lay["do_expand"]:
                 if topk_weights is not None:
                     recv_w[row] = topk_weights[t, k]

@@ -719,3 +719,97 @@ def test_prequantised_dispatch_copies_any_bytes_through_the_metadata(cm):
             assert np.array_equal(d["recv_x"][r], q[tok])
         else:
             assert not d["recv_x"][r].any()
+
+
+# ---------------------------------------------------------------------------
+# Fixed-capacity per-expert layout (low-latency kernels)
+# ---------------------------------------------------------------------------
+def _fixed_brute(idx, E, cap):
+    """Walk the slots in (t, k) order with one counter per expert."""
+    T, K = idx.shape
+    pos = [0] * E
+    dst = np.full((T, K), -1, dtype=np.int64)
+    over = False
+    for t in range(T):
+        for k in range(K):
+            e = int(idx[t, k])
+            if e < 0 or e >= E:
+                continue
+            if pos[e] < cap:
+                dst[t, k] = e * cap + pos[e]
+            else:
+                over = True
+            pos[e] += 1
+    return dst, pos, over
+
+
+@pytest.mark.parametrize("dup", [False, True])
+def test_fixed_capacity_layout_brute_force(dup):
+    rng = np.random.default_rng(71 + dup)
+    for _ in range(20):
+        R = int(rng.choice([1, 2, 4]))
+        E = R * int(rng.integers(1, 5))
+        K = int(rng.integers(1, min(E, 6) + 1)) if not dup else int(rng.integers(1, 7))
+        M = int(rng.integers(1, 9))
+        T = int(rng.integers(0, M * R + 1))
+        idx = _routing(rng, T, K, E, dup) if T > 0 else np.zeros((0, K), dtype=np.int64)
+        lay = O.layout_fixed_capacity(idx, E, R, M)
+        cap = M * R
+        dst, pos, over = _fixed_brute(idx, E, cap)
+        assert lay["capacity"] == cap and lay["rows_alloc"] == E * cap
+        assert np.array_equal(lay["dst_buffer_slot_idx"], dst)
+        assert lay["cnt_expert"].tolist() == pos
+        assert bool(lay["error"] & 2) == over
+        if not dup:
+            assert not over          # one expert per token at most: a slab never fills past T
+        meta = lay["recv_src_metadata"]
+        for t in range(T):
+            for k in range(K):
+                if dst[t, k] >= 0:
+                    assert tuple(meta[dst[t, k]]) == (t, k)
+        assert lay["row_defined"].sum() == int(np.minimum(pos, cap).sum())
+
+
+def test_fixed_capacity_matches_expanded_positions():
+    """Inside an expert, the position of every slot equals its position in
+    the expanded layout without alignment (both ascending (t, k))."""
+    rng = np.random.default_rng(73)
+    T, K, E, R, M = 300, 6, 32, 4, 80
+    idx = _routing(rng, T, K, E, dup=False)
+    fx = O.layout_fixed_capacity(idx, E, R, M)
+    ex = O.layout(idx, E, R, M, 1, True, True)
+    v = idx >= 0
+    e = np.where(v, idx, 0)
+    pos_f = fx["dst_buffer_slot_idx"] - e * fx["capacity"]
+    pos_e = ex["dst_buffer_slot_idx"] - ex["psum_expert"][e]
+    assert np.array_equal(pos_f[v], pos_e[v])
+    for key in ("cnt_expert", "psum_expert", "cnt_rank", "psum_rank", "psum_rank_src",
+                "is_token_in_rank"):
+        assert np.array_equal(fx[key], ex[key]), key
+
+
+def test_fixed_capacity_column_major_scale_index():
+    # E = 2 experts of capacity 6 (aligned to 8), H = 256 (2 blocks)
+    rows, H, cap = 12, 256, 6
+    assert O.sf_numel(rows, H, True, cap) == 2 * 2 * 8
+    assert O.sf_index(9, 1, rows, H, True, cap) == 1 * 2 * 8 + 1 * 8 + 3
+    assert O.sf_index(9, 1, rows, H, False, cap) == 9 * 2 + 1
+    ix = [O.sf_index(r, j, rows, H, True, cap) for r in range(rows) for j in range(2)]
+    assert len(set(ix)) == len(ix) and max(ix) < O.sf_numel(rows, H, True, cap)
+
+
+def test_fixed_capacity_dispatch_and_combine_round_trip():
+    """Dispatch, identity experts and the unweighted combine give x times
+    the token's number of valid slots (exact for small integers)."""
+    rng = np.random.default_rng(79)
+    T, K, E, R, M, H = 80, 4, 16, 4, 20, 128
+    idx = _routing(rng, T, K, E, dup=False)
+    lay = O.layout_fixed_capacity(idx, E, R, M)
+    x = rng.integers(-8, 9, (T, H)).astype(np.float32)
+    xb = O.f32_to_bf16_bits(x)
+    d = O.dispatch(lay, xb, None, False, False, False)
+    assert np.array_equal(d["payload_defined"], lay["row_defined"])
+    y = d["recv_x"]
+    out = O.bf16_bits_to_f32(O.combine(lay, y, None))
+    cnt = (idx >= 0).sum(1, keepdims=True)
+    assert np.array_equal(out, O.bf16_bits_to_f32(O.f32_to_bf16_bits(x * cnt)))

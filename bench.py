@@ -236,11 +236,26 @@ def recorded_traffic(kernel: str, workload: str):
 # ---------------------------------------------------------------------------
 # CPU oracle timing (cpu_baseline leg and the reference arm)
 # ---------------------------------------------------------------------------
+def oracle_layout(wl: W.Workload, idx, M: int):
+    from oracle import ep_oracle as O
+    if wl.fixed_capacity:
+        return O.layout_fixed_capacity(idx, wl.num_experts, wl.num_ranks, M)
+    return O.layout(idx, wl.num_experts, wl.num_ranks, M, wl.expert_alignment, wl.do_expand, True)
+
+
+def sample_tokens_per_rank(wl: W.Workload, T: int) -> int:
+    """M for a CPU sample of T tokens: the workload's, except that a
+    fixed-capacity sample uses the smallest capacity that holds it (the
+    oracle materialises every row of every expert's slab)."""
+    if wl.fixed_capacity:
+        return max(1, -(-T // wl.num_ranks))
+    return wl.num_max_tokens_per_rank
+
+
 def oracle_step(wl: W.Workload, inp: dict, y_bits):
     from oracle import ep_oracle as O
     idx = inp["topk_idx"].numpy()
-    lay = O.layout(idx, wl.num_experts, wl.num_ranks, wl.num_max_tokens_per_rank,
-                   wl.expert_alignment, wl.do_expand, True)
+    lay = oracle_layout(wl, idx, sample_tokens_per_rank(wl, idx.shape[0]))
     xb = inp["x"].view(torch.int16).numpy().view("uint16")
     eb = inp["expert_bias"]
     eb = None if eb is None else eb.view(torch.int16).numpy().view("uint16")
@@ -258,8 +273,7 @@ def time_oracle(wl: W.Workload, sample_tokens: int, budget_s: float, seed: int =
     T = min(sample_tokens, wl.num_tokens)
     inp = W.make_inputs(wl, seed=seed, num_tokens=T)
     # expert outputs: only the rows the routing references are materialised
-    lay0 = O.layout(inp["topk_idx"].numpy(), wl.num_experts, wl.num_ranks,
-                    wl.num_max_tokens_per_rank, wl.expert_alignment, wl.do_expand, True)
+    lay0 = oracle_layout(wl, inp["topk_idx"].numpy(), sample_tokens_per_rank(wl, T))
     dst = lay0["dst_buffer_slot_idx"]
     need = np.unique(dst[dst >= 0])
     y_bits = np.zeros((max(lay0["rows_alloc"], 1), wl.hidden), dtype=np.uint16)
@@ -278,7 +292,9 @@ def time_oracle(wl: W.Workload, sample_tokens: int, budget_s: float, seed: int =
     total = sum(by.values())
     return {"gbs": total / el / 1e9, "tokens_per_s": T / el, "sec_per_step": el, "steps": n,
             "sample": f"first {T} tokens of the {wl.name} workload (seed {seed}), full step "
-                      f"(layout + dispatch + combine) on 1 core, {n} pass(es)"}
+                      f"(layout + dispatch + combine) on 1 core, {n} pass(es)"
+                      + (f"; expert capacity {sample_tokens_per_rank(wl, T) * wl.num_ranks} "
+                         f"rows (the smallest that holds the sample)" if wl.fixed_capacity else "")}
 
 
 def bytes_from_layout(wl, T, topk_idx, lay: dict) -> dict:
@@ -311,7 +327,8 @@ def run_gpu(args, ws, rank, local):
     eb = inp["expert_bias"].to(dev) if inp["expert_bias"] is not None else None
     cfg = ep.make_config(T, wl.num_topk, wl.num_experts, wl.num_ranks, H,
                          wl.num_max_tokens_per_rank, wl.expert_alignment, wl.do_expand,
-                         wl.do_zero_padding, wl.do_cpu_sync, wl.use_fp8, wl.col_major_sf)
+                         wl.do_zero_padding, wl.do_cpu_sync, wl.use_fp8, wl.col_major_sf,
+                         fixed_capacity=wl.fixed_capacity)
     stream = torch.cuda.current_stream()
     flush_w = torch.empty(L2_FLUSH_BYTES // 4, dtype=torch.float32, device=dev)
     flush_r = torch.ones(L2_FLUSH_BYTES // 4, dtype=torch.float32, device=dev)

@@ -29,7 +29,7 @@ EP_ERR_OVERFLOW = 7
 EP_ERRBIT_BAD_TOPK_IDX = 1
 EP_ERRBIT_OVERFLOW = 2
 EP_ERRBIT_TIMEOUT = 4
-EP_ABI_VERSION = 1
+EP_ABI_VERSION = 2
 
 
 class EpError(RuntimeError):
@@ -53,7 +53,8 @@ class EpConfigC(ctypes.Structure):
         ("do_cpu_sync", ctypes.c_uint8),
         ("use_fp8", ctypes.c_uint8),
         ("use_tma_aligned_col_major_sf", ctypes.c_uint8),
-        ("reserved0", ctypes.c_uint8 * 3),
+        ("fixed_capacity", ctypes.c_uint8),
+        ("reserved0", ctypes.c_uint8 * 2),
         ("num_sms", ctypes.c_int32),
         ("cpu_sync_timeout_ms", ctypes.c_int32),
     ]
@@ -83,6 +84,8 @@ class EpLayoutInfoC(ctypes.Structure):
         ("totals", _P32),
         ("error_word", _P32),
         ("meta_rows", ctypes.c_int64),
+        ("expert_capacity", ctypes.c_int64),
+        ("sf_expert_stride", ctypes.c_int64),
     ]
 
 
@@ -140,7 +143,8 @@ def status_string(status: int) -> str:
 def make_config(num_tokens, num_topk, num_experts, num_ranks, hidden, num_max_tokens_per_rank,
                 expert_alignment=1, do_expand=False, do_zero_padding=False, do_cpu_sync=True,
                 use_fp8=False, use_tma_aligned_col_major_sf=False, num_sms=0,
-                cpu_sync_timeout_ms=0, topk_idx_is_int64=True) -> EpConfigC:
+                cpu_sync_timeout_ms=0, topk_idx_is_int64=True,
+                fixed_capacity=False) -> EpConfigC:
     c = EpConfigC()
     c.num_tokens = num_tokens
     c.num_topk = num_topk
@@ -155,6 +159,7 @@ def make_config(num_tokens, num_topk, num_experts, num_ranks, hidden, num_max_to
     c.do_cpu_sync = int(bool(do_cpu_sync))
     c.use_fp8 = int(bool(use_fp8))
     c.use_tma_aligned_col_major_sf = int(bool(use_tma_aligned_col_major_sf))
+    c.fixed_capacity = int(bool(fixed_capacity))
     c.num_sms = num_sms
     c.cpu_sync_timeout_ms = cpu_sync_timeout_ms
     return c

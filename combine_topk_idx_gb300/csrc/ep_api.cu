@@ -18,7 +18,7 @@ struct ep_handle {
   void *dmem;
   ep::LayoutParams lp;
   int64_t rows_alloc;
-  int64_t sf_hidden_stride, sf_token_stride, sf_numel;
+  int64_t sf_hidden_stride, sf_token_stride, sf_numel, sf_expert_stride;
   float *tok_scale;
 };
 
@@ -53,6 +53,12 @@ Bounds upper_bound(const ep_config &c) {
   const int64_t T = c.num_tokens, K = c.num_topk, E = c.num_experts, R = c.num_ranks;
   const int64_t L = E / R, M = c.num_max_tokens_per_rank, A = c.expert_alignment;
   Bounds b;
+  if (c.fixed_capacity) {  // every expert owns M * R rows, whatever the counts
+    b.per_rank = L * M * R;
+    b.global = E * M * R;
+    b.rows = b.global;
+    return b;
+  }
   if (c.do_expand) {
     b.per_rank = align_up(R * M * std::min(K, L) + (A - 1) * L, A);
     b.global = align_up(T * K + E * (A - 1), A);
@@ -178,6 +184,8 @@ DispatchParams dispatch_params(const ep_handle *h, const void *x, const float *t
   p.sf_src = h->tok_scale;
   p.sf_src_ts = c.hidden / 128;
   p.sf_src_hs = 1;
+  p.fixed_cap = h->lp.fixed_cap;
+  p.sf_expert_stride = h->sf_expert_stride;
   return p;
 }
 
@@ -236,9 +244,13 @@ ep_status ep_validate_config(const ep_config *c) {
     return EP_ERR_INVALID_ARG;
   if (c->topk_idx_is_int64 != 0 && c->topk_idx_is_int64 != 1) return EP_ERR_INVALID_ARG;
   if (c->do_expand > 1 || c->do_zero_padding > 1 || c->do_cpu_sync > 1 || c->use_fp8 > 1 ||
-      c->use_tma_aligned_col_major_sf > 1)
+      c->use_tma_aligned_col_major_sf > 1 || c->fixed_capacity > 1)
     return EP_ERR_INVALID_ARG;
-  if (c->reserved0[0] | c->reserved0[1] | c->reserved0[2]) return EP_ERR_INVALID_ARG;
+  if (c->reserved0[0] | c->reserved0[1]) return EP_ERR_INVALID_ARG;
+  // the fixed-capacity layout is expanded, unaligned and has no padding
+  if (c->fixed_capacity &&
+      (!c->do_expand || c->expert_alignment != 1 || c->do_zero_padding))
+    return EP_ERR_INVALID_ARG;
   if (c->num_topk > EP_MAX_TOPK || c->num_experts > EP_MAX_EXPERTS || c->hidden > EP_MAX_HIDDEN)
     return EP_ERR_UNSUPPORTED;
   const ep::Bounds b = ep::upper_bound(*c);
@@ -294,6 +306,7 @@ ep_status ep_layout(const ep_config *cfg, const void *topk_idx, ep_stream_t stre
   lp.M = c.num_max_tokens_per_rank;
   lp.A = c.expert_alignment;
   lp.do_expand = c.do_expand;
+  lp.fixed_cap = c.fixed_capacity ? c.num_max_tokens_per_rank * c.num_ranks : 0;
   // exact mode: rows never exceed the global bound; upper-bound mode: rows
   // past the allocation are dropped and flagged
   lp.row_limit = c.do_cpu_sync ? b.global : b.rows;
@@ -411,13 +424,26 @@ ep_status ep_layout(const ep_config *cfg, const void *topk_idx, ep_stream_t stre
     num_recv = slot->num_recv;
     num_exp = slot->num_expanded;
     ep::sync_pool().release(slot);
-    h->rows_alloc = c.do_expand ? num_exp : num_recv;
+    h->rows_alloc = c.fixed_capacity ? b.rows : c.do_expand ? num_exp : num_recv;
     if (err & EP_ERRBIT_BAD_TOPK_IDX) st = EP_ERR_BAD_TOPK_IDX;
   } else {
     h->rows_alloc = b.rows;
   }
   const int64_t nb = c.hidden / ep::kFp8Block;
-  if (c.use_fp8) {
+  h->sf_expert_stride = 0;
+  if (c.use_fp8 && c.fixed_capacity) {
+    const int64_t cap = lp.fixed_cap;
+    if (c.use_tma_aligned_col_major_sf) {  // one column-major slab per expert
+      h->sf_token_stride = 1;
+      h->sf_hidden_stride = align_up(cap, 4);
+      h->sf_expert_stride = nb * h->sf_hidden_stride;
+    } else {
+      h->sf_token_stride = nb;
+      h->sf_hidden_stride = 1;
+      h->sf_expert_stride = nb * cap;
+    }
+    h->sf_numel = (int64_t)c.num_experts * h->sf_expert_stride;
+  } else if (c.use_fp8) {
     if (c.use_tma_aligned_col_major_sf) {
       h->sf_token_stride = 1;
       h->sf_hidden_stride = align_up(h->rows_alloc, 4);
@@ -450,6 +476,8 @@ ep_status ep_layout(const ep_config *cfg, const void *topk_idx, ep_stream_t stre
   info->totals = lp.ctrl + ep::kCtrlNumRecv;
   info->error_word = reinterpret_cast<const uint32_t *>(lp.ctrl + ep::kCtrlError);
   info->meta_rows = lp.row_limit;
+  info->expert_capacity = lp.fixed_cap;
+  info->sf_expert_stride = h->sf_expert_stride;
   *out_handle = h;
   return st;
 }
@@ -467,7 +495,8 @@ ep_status ep_dispatch(ep_handle *h, const void *x, const float *topk_weights, vo
   } else if (recv_sf != nullptr) {
     return EP_ERR_INVALID_ARG;
   }
-  if (recv_topk_weights != nullptr && (topk_weights == nullptr || !aligned(recv_topk_weights, 4)))
+  if (recv_topk_weights != nullptr &&
+      ((T > 0 && topk_weights == nullptr) || !aligned(recv_topk_weights, 4)))
     return EP_ERR_INVALID_ARG;
   if (topk_weights != nullptr && !aligned(topk_weights, 4)) return EP_ERR_INVALID_ARG;
   if (recv_topk_idx != nullptr && (c.do_expand || !aligned(recv_topk_idx, 4)))
@@ -498,7 +527,8 @@ ep_status ep_dispatch_fp8(ep_handle *h, const void *x_fp8, const float *x_sf,
   if (h->rows_alloc > 0 && (recv_x == nullptr || !aligned(recv_x, 16) || recv_sf == nullptr ||
                             !aligned(recv_sf, 4)))
     return EP_ERR_INVALID_ARG;
-  if (recv_topk_weights != nullptr && (topk_weights == nullptr || !aligned(recv_topk_weights, 4)))
+  if (recv_topk_weights != nullptr &&
+      ((T > 0 && topk_weights == nullptr) || !aligned(recv_topk_weights, 4)))
     return EP_ERR_INVALID_ARG;
   if (topk_weights != nullptr && !aligned(topk_weights, 4)) return EP_ERR_INVALID_ARG;
   if (recv_topk_idx != nullptr && (c.do_expand || !aligned(recv_topk_idx, 4)))

@@ -335,19 +335,13 @@ __global__ void __launch_bounds__(kMaxConsumers + 32, 1) dispatch_kernel(Dispatc
 
 // Column-major scale factors of every destination row, gathered from the
 // per-token scales (sf_src: the dispatch kernel's own, or the caller's for a
-// pre-quantised input) through the row's source token (recv_src_metadata).  Grid
-// (row blocks, groups of 4 scale blocks): thread (row, g) loads 16 bytes of
-// its token's scales and writes scale blocks 4g..4g+3 of its row, so for
-// each block the threads of a warp write 32 consecutive rows.  Padding rows
-// get 0.
-__global__ void __launch_bounds__(256) sf_expand_kernel(DispatchParams p) {
-  griddep_wait();  // the per-token scales come from the dispatch kernel
-  const int nb = p.H / kFp8Block;
-  const int64_t total = min((int64_t)__ldg(p.num_rows), p.rows_alloc);
-  const int64_t row = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
-  if (row >= total) return;
-  const int j0 = blockIdx.y * 4;
-  const int tok = __ldg(&reinterpret_cast<const int2 *>(p.meta)[row].x);
+// pre-quantised input) through the row's source token (recv_src_metadata).
+// One work item (row, g) loads 16 bytes of its token's scales and writes
+// scale blocks 4g..4g+3 of its row; the threads of a warp take 32
+// consecutive rows of one g, so every store of a warp is contiguous.
+// Padding rows get 0.
+__device__ __forceinline__ void sf_expand_one(const DispatchParams &p, int nb, int j0, int tok,
+                                              float *dst) {
   float v[4] = {0.f, 0.f, 0.f, 0.f};
   if (tok >= 0) {
     const float *src = p.sf_src + (int64_t)tok * p.sf_src_ts + (int64_t)j0 * p.sf_src_hs;
@@ -358,10 +352,40 @@ __global__ void __launch_bounds__(256) sf_expand_kernel(DispatchParams p) {
       for (int u = 0; u < 4 && j0 + u < nb; ++u) v[u] = __ldg(src + (int64_t)u * p.sf_src_hs);
     }
   }
-  float *dst = p.recv_sf + row + (int64_t)j0 * p.sf_hidden_stride;
 #pragma unroll
   for (int u = 0; u < 4; ++u)
     if (j0 + u < nb) dst[(int64_t)u * p.sf_hidden_stride] = v[u];
+}
+
+__global__ void __launch_bounds__(256) sf_expand_kernel(DispatchParams p) {
+  griddep_wait();  // the per-token scales come from the dispatch kernel
+  const int nb = p.H / kFp8Block;
+  const int2 *meta = reinterpret_cast<const int2 *>(p.meta);
+  if (p.fixed_cap > 0) {
+    // grid (x, 1, E): the CTAs of expert e walk its used rows i < count,
+    // group of 4 scale blocks by group, consecutive threads on consecutive
+    // rows of one group (coalesced stores into the expert's column-major slab)
+    const int e = blockIdx.z;
+    const int64_t n = min((int64_t)__ldg(p.cnt_e + e), (int64_t)p.fixed_cap);
+    const int64_t items = n * ((nb + 3) / 4);
+    const int64_t row0 = (int64_t)e * p.fixed_cap;
+    float *out0 = p.recv_sf + (int64_t)e * p.sf_expert_stride;
+    for (int64_t it = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; it < items;
+         it += (int64_t)gridDim.x * blockDim.x) {
+      const int64_t g = it / n, i = it - g * n;
+      const int j0 = (int)g * 4;
+      sf_expand_one(p, nb, j0, __ldg(&meta[row0 + i].x),
+                    out0 + i + (int64_t)j0 * p.sf_hidden_stride);
+    }
+    return;
+  }
+  // one global column-major matrix over the rows below the layout's total:
+  // grid (row blocks, groups of 4 scale blocks)
+  const int64_t n = min((int64_t)__ldg(p.num_rows), p.rows_alloc);
+  const int64_t row = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
+  if (row >= n) return;
+  const int j0 = blockIdx.y * 4;
+  sf_expand_one(p, nb, j0, __ldg(&meta[row].x), p.recv_sf + row + (int64_t)j0 * p.sf_hidden_stride);
 }
 
 template <int MODE, bool CM>
@@ -404,13 +428,19 @@ cudaError_t launch_one(const DispatchParams &p0, int sm_cap, cudaStream_t s) {
   err = cudaGetLastError();
   if (err != cudaSuccess || MODE == kModeBf16 || !CM) return err;
   // column-major scales: one gather pass (rows past the real total, in an
-  // upper-bound allocation, are left untouched)
-  const int64_t sf_grid = (p.rows_alloc + 255) / 256;
+  // upper-bound allocation, are left untouched; so are the unused rows of a
+  // fixed-capacity slab)
   const int groups = (H / kFp8Block + 3) / 4;
-  if (sf_grid > 0) {
+  dim3 sf_grid;
+  if (p.fixed_cap > 0)  // per expert: up to 4 CTAs striding over its (row, group) items
+    sf_grid = dim3((unsigned)std::min<int64_t>(4, ((int64_t)p.fixed_cap * groups + 2047) / 2048), 1,
+                   (unsigned)p.E);
+  else
+    sf_grid = dim3((unsigned)((p.rows_alloc + 255) / 256), (unsigned)groups);
+  if (p.rows_alloc > 0) {
     // launched while the dispatch kernel drains; it waits on griddepcontrol
     cudaLaunchConfig_t lc{};
-    lc.gridDim = dim3((unsigned)sf_grid, (unsigned)groups);
+    lc.gridDim = sf_grid;
     lc.blockDim = dim3(256);
     lc.stream = s;
     cudaLaunchAttribute attr[1];

@@ -30,6 +30,7 @@ struct LayoutParams {
   int idx_is_int64;
   int T, K, E, R, L, M, A;
   int do_expand;
+  int fixed_cap;          // > 0: fixed-capacity layout, rows per expert (do_expand only)
   int num_blocks;         // layout grid (one CTA per chunk of tokens)
   int blocks_per_src;     // chunks per source rank
   int chunk_tokens;       // tokens per chunk
@@ -80,6 +81,10 @@ struct DispatchParams {
   const float *sf_src;
   int64_t sf_src_ts, sf_src_hs;
   int sf_src_vec4;
+  // fixed-capacity layout: rows per expert (0 otherwise) and the scale stride
+  // between experts' column-major slabs
+  int fixed_cap;
+  int64_t sf_expert_stride;
 };
 
 struct CombineParams {

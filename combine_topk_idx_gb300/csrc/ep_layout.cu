@@ -266,11 +266,17 @@ __global__ void __launch_bounds__(NT) layout_assign_kernel(LayoutParams p) {
   }
   __syncthreads();
 
-  // Segment starts of the sort key (aligned expert counts, or rank counts).
-  if (p.do_expand)
+  // Segment starts of the sort key (aligned expert counts, rank counts, or
+  // the fixed per-expert capacity).
+  const int fcap = p.fixed_cap;
+  if (fcap > 0) {
+    for (int e = threadIdx.x; e <= E; e += NT) seg_s[e] = e * fcap;
+    __syncthreads();
+  } else if (p.do_expand) {
     cta_exclusive_scan(E, [&](int e) { return (tot_s[e] + A - 1) / A * A; }, seg_s, warp_tot);
-  else
+  } else {
     cta_exclusive_scan(R, [&](int r) { return tot_s[E + r]; }, seg_s, warp_tot);
+  }
 
   if (b == 0) {
     // Global outputs, written once by CTA 0.  The sort key's prefix sum is
@@ -283,14 +289,22 @@ __global__ void __launch_bounds__(NT) layout_assign_kernel(LayoutParams p) {
       p.cnt_e_al[e] = (tot_s[e] + A - 1) / A * A;
     }
     for (int r = threadIdx.x; r < R; r += NT) p.cnt_r[r] = tot_s[E + r];
-    if (p.do_expand) {
+    if (fcap > 0) {
+      // psum_expert stays the prefix of the counts (written by warp 0)
+    } else if (p.do_expand) {
       for (int e = threadIdx.x; e <= E; e += NT) p.psum_e[e] = seg_s[e];
     } else {
       for (int r = threadIdx.x; r <= R; r += NT) p.psum_r[r] = seg_s[r];
     }
     if (warp == 0) {
       int num_expanded, num_recv;
-      if (p.do_expand) {
+      bool over = false;
+      if (fcap > 0) {
+        num_expanded = warp_exclusive_scan(E, [&](int e) { return tot_s[e]; }, p.psum_e);
+        num_recv = warp_exclusive_scan(R, [&](int r) { return tot_s[E + r]; }, p.psum_r);
+        for (int e = lane; e < E; e += 32) over |= tot_s[e] > fcap;
+        over = __any_sync(0xffffffffu, over);
+      } else if (p.do_expand) {
         num_expanded = seg_s[E];
         num_recv = warp_exclusive_scan(R, [&](int r) { return tot_s[E + r]; }, p.psum_r);
       } else {
@@ -303,7 +317,7 @@ __global__ void __launch_bounds__(NT) layout_assign_kernel(LayoutParams p) {
       err = __reduce_or_sync(0xffffffffu, err);
       if (lane == 0) {
         const int64_t total_rows = p.do_expand ? num_expanded : num_recv;
-        if (total_rows > p.row_limit) err |= EP_ERRBIT_OVERFLOW;
+        if (fcap > 0 ? over : total_rows > p.row_limit) err |= EP_ERRBIT_OVERFLOW;
         p.ctrl[kCtrlError] = static_cast<int>(err);
         p.ctrl[kCtrlNumRecv] = num_recv;
         p.ctrl[kCtrlNumExpanded] = num_expanded;
@@ -430,12 +444,17 @@ __global__ void __launch_bounds__(NT) layout_assign_kernel(LayoutParams p) {
         }
       }
     }
+    bool keep = own >= 0 && own < p.row_limit;
+    if (fcap > 0 && own >= 0 && own >= (e + 1) * fcap) {  // past the expert's capacity
+      row = -1;
+      keep = false;
+    }
     if (row >= p.row_limit) row = -1;
     p.dst[base + i] = row;
-    if (own >= 0 && own < p.row_limit) meta[own] = make_int2(t0 + tl, k);
+    if (keep) meta[own] = make_int2(t0 + tl, k);
   }
 
-  if (p.do_expand) {
+  if (p.do_expand && fcap == 0) {
     // alignment padding rows -> (-1, -1): one warp per expert, experts
     // b + (warp + NWARPS * i) * gridDim.x
     for (int e = b + warp * (int)gridDim.x; e < E; e += NWARPS * (int)gridDim.x) {

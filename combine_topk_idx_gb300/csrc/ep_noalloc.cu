@@ -69,6 +69,7 @@ extern "C" ep_status ep_layout_noalloc(const ep_config *cfg, const void *topk_id
   lp.M = c.num_max_tokens_per_rank;
   lp.A = c.expert_alignment;
   lp.do_expand = c.do_expand;
+  lp.fixed_cap = c.fixed_capacity ? c.num_max_tokens_per_rank * c.num_ranks : 0;
   lp.row_limit = rows;
   lp.chunk_tokens = ep::kLayoutChunkTokens;
   const int64_t src_ranks = ((int64_t)T + lp.M - 1) / lp.M;

@@ -56,6 +56,7 @@ class Workload:
     do_zero_padding: bool = False
     do_cpu_sync: bool = True
     expert_bias_std: float = 0.0  # >0: per-expert BF16 bias [E, H] ~ N(0, std)
+    fixed_capacity: bool = False  # fixed-capacity per-expert layout (M * R rows per expert)
 
 
 WORKLOADS = {
@@ -69,6 +70,9 @@ WORKLOADS = {
                         do_expand=True, do_zero_padding=True, do_cpu_sync=True),
     "skewed": Workload("skewed", 16384, 4096, 64, 8, 6, 2048, 1, "zipf", drop_prob=0.02,
                        zipf_s=1.2, do_expand=False, do_cpu_sync=True, expert_bias_std=0.1),
+    "decode_ll": Workload("decode_ll", 1024, 7168, 256, 8, 8, 128, 1, "uniform",
+                          use_fp8=True, col_major_sf=True, do_expand=True, do_cpu_sync=False,
+                          fixed_capacity=True),
     "large": Workload("large", 32768, 7168, 256, 32, 8, 1024, 128, "softmax",
                       use_fp8=True, col_major_sf=True, do_expand=True,
                       do_zero_padding=True, do_cpu_sync=False),

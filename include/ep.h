@@ -66,7 +66,8 @@ typedef enum ep_status {
 
 /* Bits of the device error word (ep_layout_info.error_word). */
 #define EP_ERRBIT_BAD_TOPK_IDX 1u  /* value outside [-1, E): the slot is treated as empty */
-#define EP_ERRBIT_OVERFLOW 2u      /* rows at or past rows_alloc were dropped */
+#define EP_ERRBIT_OVERFLOW 2u      /* rows at or past rows_alloc (or past an expert's
+                                      fixed capacity) were dropped */
 #define EP_ERRBIT_TIMEOUT 4u       /* a bounded device-side wait gave up (output undefined) */
 
 /* Build limits (checked by ep_validate_config). */
@@ -94,10 +95,28 @@ typedef struct ep_config {
   uint8_t do_cpu_sync;              /* 1: wait for the counts, exact allocation */
   uint8_t use_fp8;                  /* dispatch quantises to e4m3 + fp32 scales */
   uint8_t use_tma_aligned_col_major_sf; /* FP8 scales column-major, 16 B aligned */
-  uint8_t reserved0[3];             /* must be 0 */
+  uint8_t fixed_capacity;           /* 1: fixed-capacity per-expert layout (below) */
+  uint8_t reserved0[2];             /* must be 0 */
   int32_t num_sms;                  /* 0 = all SMs; otherwise cap on the SMs used */
   int32_t cpu_sync_timeout_ms;      /* do_cpu_sync deadline; 0 = 10000 ms */
 } ep_config;
+
+/*
+ * Fixed-capacity per-expert layout (fixed_capacity = 1; DeepEP README,
+ * "Interfaces and examples", low_latency_dispatch: a per-rank
+ * [local experts, max tokens per rank * ranks, hidden] receive tensor and a
+ * per-expert count, usable under CUDA graphs).  Requires do_expand = 1,
+ * expert_alignment = 1, do_zero_padding = 0 and E * M * R < 2^31.  With
+ * capacity = M * R, expert e owns rows [e * capacity, (e + 1) * capacity):
+ * its i-th slot in (token, slot) order lands at row e * capacity + i, and
+ * rows past cnt_expert[e] are not written.  rows_alloc = E * capacity in
+ * both sync modes.  A slot whose position reaches the capacity (only when a
+ * token repeats an expert) is dropped and sets EP_ERRBIT_OVERFLOW.  FP8
+ * scales: row-major [E * capacity, H/128], or, with
+ * use_tma_aligned_col_major_sf, one column-major slab per expert --
+ * sf[e * sf_expert_stride + j * sf_hidden_stride + i], sf_hidden_stride =
+ * align(capacity, 4), sf_expert_stride = (H/128) * sf_hidden_stride.
+ */
 
 /*
  * Filled by ep_layout.  Device pointers are owned by the handle and stay
@@ -124,6 +143,10 @@ typedef struct ep_layout_info {
   const int32_t *totals;              /* [2] device num_recv_tokens, num_expanded_tokens */
   const uint32_t *error_word;         /* [1] EP_ERRBIT_* bits */
   int64_t meta_rows;                  /* rows of recv_src_metadata */
+  int64_t expert_capacity;            /* fixed_capacity: rows per expert, else 0 */
+  int64_t sf_expert_stride;           /* fixed_capacity: the scales of row e * capacity + i
+                                         are recv_sf[e * sf_expert_stride + i *
+                                         sf_token_stride + j * sf_hidden_stride]; else 0 */
 } ep_layout_info;
 
 typedef struct ep_handle ep_handle;
@@ -157,7 +180,8 @@ EP_API ep_status ep_layout(const ep_config *cfg, const void *topk_idx, ep_stream
  * ep_dispatch -- copy epilogue (§7.3 launch_dispatch_copy_epilogue, §7.4).
  *
  * x: device BF16 [T, H], 16-byte aligned.
- * topk_weights: device fp32 [T, K] or NULL (then recv_topk_weights must be NULL).
+ * topk_weights: device fp32 [T, K] or NULL (then recv_topk_weights must be NULL,
+ *   unless T = 0).
  * recv_x: [rows_alloc, H] BF16, or e4m3 bytes when cfg->use_fp8; 16-byte aligned.
  * recv_sf: FP8 only, fp32 [sf_numel]; row-major [rows_alloc, H/128] or, with
  *   use_tma_aligned_col_major_sf, column-major with hidden stride
@@ -361,7 +385,7 @@ EP_API ep_status ep_upper_bound_rows(const ep_config *cfg, int64_t *rows);
 EP_API ep_status ep_host_wait_flag(const volatile int32_t *flag, int32_t expected,
                             int32_t timeout_ms);
 
-#define EP_ABI_VERSION 1
+#define EP_ABI_VERSION 2
 
 #ifdef __cplusplus
 }

@@ -18,12 +18,16 @@ def cfg_for(ep, wl: W.Workload, T: int | None = None, **over):
     M = over.pop("M", max(wl.num_max_tokens_per_rank, -(-T // wl.num_ranks)))
     kw = dict(expert_alignment=wl.expert_alignment, do_expand=wl.do_expand,
               do_zero_padding=wl.do_zero_padding, do_cpu_sync=wl.do_cpu_sync,
-              use_fp8=wl.use_fp8, use_tma_aligned_col_major_sf=wl.col_major_sf)
+              use_fp8=wl.use_fp8, use_tma_aligned_col_major_sf=wl.col_major_sf,
+              fixed_capacity=wl.fixed_capacity)
     kw.update(over)
     return ep.make_config(T, wl.num_topk, wl.num_experts, wl.num_ranks, wl.hidden, M, **kw)
 
 
 def oracle_layout(cfg, topk_idx: np.ndarray) -> dict:
+    if getattr(cfg, "fixed_capacity", 0):
+        return O.layout_fixed_capacity(topk_idx, cfg.num_experts, cfg.num_ranks,
+                                       cfg.num_max_tokens_per_rank)
     return O.layout(topk_idx, cfg.num_experts, cfg.num_ranks, cfg.num_max_tokens_per_rank,
                     cfg.expert_alignment, bool(cfg.do_expand), bool(cfg.do_cpu_sync))
 
@@ -48,8 +52,12 @@ def check_layout(h, lay: dict, g: dict | None = None) -> dict:
     assert np.array_equal(g["psum_rank_src"], lay["psum_rank_src"]), "psum_rank_src"
     assert np.array_equal(g["is_token_in_rank"].astype(bool), lay["is_token_in_rank"]), "in_rank"
     assert np.array_equal(g["dst_buffer_slot_idx"], lay["dst_buffer_slot_idx"]), "dst"
-    n = min(lay["total_rows"], lay["rows_alloc"])
-    assert np.array_equal(g["recv_src_metadata"][:n], lay["recv_src_metadata"][:n]), "meta"
+    if "row_defined" in lay:     # fixed capacity: only each expert's used rows
+        d = lay["row_defined"]
+        assert np.array_equal(g["recv_src_metadata"][d], lay["recv_src_metadata"][d]), "meta"
+    else:
+        n = min(lay["total_rows"], lay["rows_alloc"])
+        assert np.array_equal(g["recv_src_metadata"][:n], lay["recv_src_metadata"][:n]), "meta"
     assert g["totals"].tolist() == [lay["num_recv_tokens"], lay["num_expanded_tokens"]]
     assert int(g["error_word"][0]) == lay["error"], "error word"
     assert h.rows_alloc == lay["rows_alloc"], "rows_alloc"
@@ -81,7 +89,7 @@ def check_dispatch(h, lay: dict, d_or: dict, out: dict, use_fp8: bool, col_major
             gs = out["recv_sf"].cpu().numpy()
             rows = np.flatnonzero(pdef)
             for j in range(nb):
-                ix = O.sf_index(rows, j, rows_alloc, H, col_major)
+                ix = O.sf_index(rows, j, rows_alloc, H, col_major, lay.get("capacity"))
                 assert np.array_equal(gs[ix], d_or["recv_sf"][ix]), f"recv_sf block {j}"
         mdef = d_or["meta_defined"][:rows_alloc]
         if out.get("recv_topk_weights") is not None:
@@ -102,7 +110,8 @@ def check_dispatch(h, lay: dict, d_or: dict, out: dict, use_fp8: bool, col_major
             gx = out["recv_x"].index_select(0, ri).cpu().numpy()
             assert np.all(gx == d_or["q"][i][None, :]), f"token {t} payload"
             nb = H // 128
-            ix = np.stack([O.sf_index(np.array(rows), j, rows_alloc, H, col_major)
+            ix = np.stack([O.sf_index(np.array(rows), j, rows_alloc, H, col_major,
+                                      lay.get("capacity"))
                            for j in range(nb)], 1)
             gs = out["recv_sf"][torch.from_numpy(ix.reshape(-1)).to(ri.device)].cpu().numpy()
             assert np.array_equal(gs.reshape(len(rows), nb),

@@ -62,8 +62,10 @@ int main(void) {
   printf("ep_layout_buffers size %zu\n", sizeof(ep_layout_buffers));
   P(ep_config, num_tokens) P(ep_config, topk_idx_is_int64) P(ep_config, do_expand)
   P(ep_config, use_tma_aligned_col_major_sf) P(ep_config, num_sms) P(ep_config, cpu_sync_timeout_ms)
+  P(ep_config, fixed_capacity) P(ep_config, reserved0)
   P(ep_layout_info, rows_alloc) P(ep_layout_info, topk_idx) P(ep_layout_info, error_word)
-  P(ep_layout_info, meta_rows) P(ep_layout_buffers, status)
+  P(ep_layout_info, meta_rows) P(ep_layout_info, expert_capacity)
+  P(ep_layout_info, sf_expert_stride) P(ep_layout_buffers, status)
   return 0;
 }
 '''
@@ -83,9 +85,10 @@ int main(void) {
     assert got[("ep_layout_info", "size")] == ctypes.sizeof(I)
     assert got[("ep_layout_buffers", "size")] == ctypes.sizeof(B)
     for f in ("num_tokens", "topk_idx_is_int64", "do_expand", "use_tma_aligned_col_major_sf",
-              "num_sms", "cpu_sync_timeout_ms"):
+              "num_sms", "cpu_sync_timeout_ms", "fixed_capacity", "reserved0"):
         assert got[("ep_config", f)] == getattr(C, f).offset, f
-    for f in ("rows_alloc", "topk_idx", "error_word", "meta_rows"):
+    for f in ("rows_alloc", "topk_idx", "error_word", "meta_rows", "expert_capacity",
+              "sf_expert_stride"):
         assert got[("ep_layout_info", f)] == getattr(I, f).offset, f
     assert got[("ep_layout_buffers", "status")] == B.status.offset
 
@@ -116,6 +119,16 @@ def _cfg(ep, **kw):
     ({"num_max_tokens_per_rank": 0}, 1),
     ({"num_sms": -3}, 1),
     ({"cpu_sync_timeout_ms": -1}, 1),
+    ({"fixed_capacity": True, "do_expand": True, "expert_alignment": 1,
+      "do_zero_padding": False}, 0),
+    ({"fixed_capacity": True, "do_expand": False, "expert_alignment": 1}, 1),
+    ({"fixed_capacity": True, "do_expand": True, "expert_alignment": 8,
+      "do_zero_padding": False}, 1),                # no alignment in the fixed layout
+    ({"fixed_capacity": True, "do_expand": True, "expert_alignment": 1,
+      "do_zero_padding": True}, 1),
+    ({"fixed_capacity": True, "do_expand": True, "expert_alignment": 1, "do_zero_padding": False,
+      "num_experts": 2048, "num_ranks": 16, "num_tokens": 16384,
+      "num_max_tokens_per_rank": 65536}, 2),       # E * M * R rows past int32
 ])
 def test_validate_config(ep, kw, status):
     assert ep.validate_config(_cfg(ep, **kw)) == status
@@ -127,6 +140,9 @@ def test_validate_rejects_bad_flags_and_reserved(ep):
     assert ep.validate_config(c) == ep.EP_ERR_INVALID_ARG
     c = _cfg(ep)
     c.reserved0[1] = 7
+    assert ep.validate_config(c) == ep.EP_ERR_INVALID_ARG
+    c = _cfg(ep, do_zero_padding=False, expert_alignment=1)
+    c.fixed_capacity = 2
     assert ep.validate_config(c) == ep.EP_ERR_INVALID_ARG
     c = _cfg(ep)
     c.topk_idx_is_int64 = 5
@@ -146,6 +162,8 @@ def test_upper_bound_rows_match_oracle(ep):
         for de in (False, True):
             c = ep.make_config(T, K, E, R, 128, M, A, de)
             assert ep.upper_bound_rows(c) == O.upper_bound_rows(T, K, E, R, M, A, de)
+        c = ep.make_config(T, K, E, R, 128, M, 1, True, fixed_capacity=True)
+        assert ep.upper_bound_rows(c) == E * M * R
 
 
 def test_host_wait_flag_deadline(ep):

@@ -86,7 +86,7 @@ def run_prequant(ep, cfg, idx_cpu, w_cpu, col_major_input, seed=3, canary=4):
     pdef = np.flatnonzero(d_or["payload_defined"][:rows])
     gs = out["recv_sf"].cpu().numpy().view(np.uint32)
     for j in range(nb):
-        ix = O.sf_index(pdef, j, rows, H, cm)
+        ix = O.sf_index(pdef, j, rows, H, cm, lay.get("capacity"))
         assert np.array_equal(gs[ix], d_or["recv_sf"][ix].view(np.uint32)), f"sf bits block {j}"
     assert bool((big_x[rows:] == 0xA5).all()), "payload written past rows_alloc"
     assert bool((big_sf[sfn:] == -7.0).all()), "scales written past sf_numel"

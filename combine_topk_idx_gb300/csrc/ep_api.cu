@@ -70,6 +70,27 @@ Bounds upper_bound(const ep_config &c) {
   return b;
 }
 
+// Polls the three tagged words of `slot` until each carries `seq` (or the
+// deadline passes); returns their values in words[0..2].
+ep_status wait_host_words(const HostSync *slot, int32_t seq, int32_t timeout_ms,
+                          uint64_t words[3]) {
+  const uint64_t tag = (uint64_t)(uint32_t)seq;
+  const volatile uint64_t *src[3] = {&slot->num_recv, &slot->num_expanded, &slot->error};
+  const auto deadline = std::chrono::steady_clock::now() + std::chrono::milliseconds(timeout_ms);
+  int got = 0;
+  for (uint64_t spin = 0;; ++spin) {
+    while (got < 3) {
+      const uint64_t v =
+          __atomic_load_n(const_cast<const uint64_t *>(src[got]), __ATOMIC_ACQUIRE);
+      if ((v >> 32) != tag) break;
+      words[got++] = v;
+    }
+    if (got == 3) return EP_OK;
+    if ((spin & 255) == 0 && std::chrono::steady_clock::now() >= deadline) return EP_ERR_TIMEOUT;
+    if (spin > 4096) std::this_thread::yield();
+  }
+}
+
 // Pool of pinned, device-mapped host words for the count wait.
 struct SyncPool {
   std::mutex mu;
@@ -384,7 +405,7 @@ ep_status ep_layout(const ep_config *cfg, const void *topk_idx, ep_stream_t stre
     int32_t seq = 0;
     slot = ep::sync_pool().acquire(&seq);
     if (slot == nullptr) return fail(EP_ERR_OOM);
-    slot->flag = 0;
+    slot->num_recv = slot->num_expanded = slot->error = 0;
     void *dptr = nullptr;
     ce = cudaHostGetDevicePointer(&dptr, (void *)slot, 0);
     if (ce != cudaSuccess) {
@@ -414,15 +435,16 @@ ep_status ep_layout(const ep_config *cfg, const void *topk_idx, ep_stream_t stre
   int64_t num_recv = -1, num_exp = -1;
   if (c.do_cpu_sync) {
     const int32_t timeout = c.cpu_sync_timeout_ms > 0 ? c.cpu_sync_timeout_ms : 10000;
-    const ep_status w = ep_host_wait_flag(&slot->flag, lp.seq, timeout);
+    uint64_t words[3];
+    const ep_status w = ep::wait_host_words(slot, lp.seq, timeout, words);
     if (w != EP_OK) {
       // the slot may still be written later: leave it out of the pool
       delete h;
       return fail(w);
     }
-    const int32_t err = slot->error;
-    num_recv = slot->num_recv;
-    num_exp = slot->num_expanded;
+    num_recv = (uint32_t)words[0];
+    num_exp = (uint32_t)words[1];
+    const uint32_t err = (uint32_t)words[2];
     ep::sync_pool().release(slot);
     h->rows_alloc = c.fixed_capacity ? b.rows : c.do_expand ? num_exp : num_recv;
     if (err & EP_ERRBIT_BAD_TOPK_IDX) st = EP_ERR_BAD_TOPK_IDX;

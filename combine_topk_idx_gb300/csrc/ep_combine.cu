@@ -33,6 +33,8 @@ namespace {
 
 constexpr int kStages = 3;
 constexpr int kMaxConsumers = 224;
+constexpr int64_t kStageBudget = 96 * 1024;    // shared-memory stages per CTA
+constexpr int64_t kEbStageBudget = 48 * 1024;  // same, with a per-expert bias
 constexpr int kWaitIters = 4000;          // x kWaitHintNs: gives up after ~2 s
 constexpr uint32_t kWaitHintNs = 500000;
 
@@ -228,13 +230,18 @@ cudaError_t launch_one(const CombineParams &p, int sm_cap, cudaStream_t s) {
   const int64_t row_bytes = 2 * (int64_t)p.H;
   const int nbias = (p.bias0 != nullptr) + (p.bias1 != nullptr);
   const int slots_cap = p.K + nbias;
-  // Stage budget ~96 KB per CTA (two CTAs per SM); chunks are equal-sized
-  // multiples of 16 bytes.
-  const int64_t budget = 96 * 1024 / kStages;
-  int64_t chunk = std::max<int64_t>(16, budget / slots_cap / 16 * 16);
+  // Stage budget ~96 KB per CTA (two CTAs per SM).  With a per-expert bias
+  // half of it: the bias rows are read through L1, which keeps what shared
+  // memory leaves free.  Chunks are equal-sized multiples of 512 bytes where
+  // the row allows (whole L2 lines for the bias reads), else of 16 bytes.
+  const int64_t budget = (EB ? kEbStageBudget : kStageBudget) / kStages;
+  const int64_t gran = row_bytes >= 512 ? 512 : 16;
+  int64_t chunk = std::max<int64_t>(gran, budget / slots_cap / gran * gran);
   chunk = std::min(chunk, row_bytes);
-  const int nchunks = (int)((row_bytes + chunk - 1) / chunk);
-  chunk = ((row_bytes + nchunks - 1) / nchunks + 15) / 16 * 16;
+  const int64_t n0 = (row_bytes + chunk - 1) / chunk;
+  chunk = std::min(row_bytes, ((row_bytes + n0 - 1) / n0 + gran - 1) / gran * gran);
+  chunk = (chunk + 15) / 16 * 16;
+  const int nchunks = (int)((row_bytes + chunk - 1) / chunk);  // every chunk non-empty
   const int nv = (int)(chunk / 16);
   const int consumers = std::min(kMaxConsumers, (nv + 31) / 32 * 32);
   const int threads = consumers + 32;

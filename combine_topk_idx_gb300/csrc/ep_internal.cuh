@@ -16,12 +16,15 @@ constexpr int kLayoutChunkTokens = 256;  // tokens per layout chunk (<= 8192 slo
 enum CtrlSlot { kCtrlError = 0, kCtrlNumRecv = 2, kCtrlNumExpanded = 3, kCtrlWords = 8 };
 
 // Pinned, device-mapped host words the count wait polls (do_cpu_sync).
+// Mapped host words of the count wait.  Each word is (seq << 32 | value):
+// it is current once its high half equals the call's sequence number, so the
+// device needs no fence to order them and the host reads each word whole
+// (aligned 8-byte accesses are single-copy atomic).
 struct HostSync {
-  volatile int32_t flag;
-  volatile int32_t error;
-  volatile int32_t num_recv;
-  volatile int32_t num_expanded;
-  int32_t pad[12];
+  volatile uint64_t num_recv;
+  volatile uint64_t num_expanded;
+  volatile uint64_t error;
+  uint64_t pad[5];
 };
 
 // Everything a layout kernel needs; passed by value.

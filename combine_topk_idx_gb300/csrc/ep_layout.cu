@@ -14,7 +14,9 @@
 //            and the totals of the chunks before it), scans them into segment
 //            starts, then ranks its own slots stably: warps walk contiguous
 //            runs of (token, slot) pairs in order, ranking equal keys with
-//            __match_any_sync.  Row = segment start + earlier chunks +
+//            shared 64-bit words (a running count plus the mask of the lanes
+//            holding the key in the current step).  Row = segment start +
+//            earlier chunks +
 //            earlier warps + earlier lanes, i.e. ascending (token, slot)
 //            inside every segment, with no atomics deciding positions.  CTA 0
 //            also writes the global counts and prefix sums (and, for the
@@ -125,17 +127,32 @@ __global__ void __launch_bounds__(NTC) layout_count_kernel(LayoutParams p) {
   for (int i = threadIdx.x; i < E + R; i += NTC) smem[i] = 0;
   for (int e = threadIdx.x; e < E; e += NTC) rank_of[e] = e / L;
 
-  // Coalesced load of the chunk: validate and keep an int32 copy.
+  // Coalesced load of the chunk, eight loads in flight per thread: validate
+  // and keep an int32 copy.
   unsigned err = 0;
-  for (int i = threadIdx.x; i < ns; i += NTC) {
-    long long v = p.idx_is_int64 ? __ldg(static_cast<const long long *>(p.topk_idx) + base + i)
-                                 : __ldg(static_cast<const int *>(p.topk_idx) + base + i);
-    if (v < -1 || v >= E) {
-      err |= EP_ERRBIT_BAD_TOPK_IDX;
-      v = -1;
+  constexpr int kBatch = 8;
+  for (int i0 = threadIdx.x; i0 < ns; i0 += NTC * kBatch) {
+    long long v[kBatch];
+#pragma unroll
+    for (int u = 0; u < kBatch; ++u) {
+      const int i = i0 + u * NTC;
+      v[u] = -1;
+      if (i < ns)
+        v[u] = p.idx_is_int64 ? __ldg(static_cast<const long long *>(p.topk_idx) + base + i)
+                              : __ldg(static_cast<const int *>(p.topk_idx) + base + i);
     }
-    idx_s[i] = static_cast<int>(v);
-    p.topk32[base + i] = static_cast<int>(v);
+#pragma unroll
+    for (int u = 0; u < kBatch; ++u) {
+      const int i = i0 + u * NTC;
+      if (i >= ns) break;
+      long long x = v[u];
+      if (x < -1 || x >= E) {
+        err |= EP_ERRBIT_BAD_TOPK_IDX;
+        x = -1;
+      }
+      idx_s[i] = static_cast<int>(x);
+      p.topk32[base + i] = static_cast<int>(x);
+    }
   }
   err = __reduce_or_sync(0xffffffffu, err);
   __syncthreads();
@@ -195,7 +212,7 @@ __global__ void __launch_bounds__(NTC) layout_count_kernel(LayoutParams p) {
   if (threadIdx.x == 0) p.blk_err[b] = err_s;
 }
 
-__global__ void __launch_bounds__(NT) layout_assign_kernel(LayoutParams p) {
+__global__ void __launch_bounds__(NT, 1) layout_assign_kernel(LayoutParams p) {
   extern __shared__ __align__(16) int smem[];
   const int K = p.K, L = p.L, E = p.E, R = p.R, A = p.A;
   const int nkey = p.do_expand ? E : R;
@@ -266,6 +283,23 @@ __global__ void __launch_bounds__(NT) layout_assign_kernel(LayoutParams p) {
   }
   __syncthreads();
 
+  // psum_rank_src[r][s], the tokens of source ranks < s that rank r
+  // receives, is the rank total of the chunks before source rank s's first
+  // chunk: that chunk's CTA holds it in bef_s.  Source ranks without tokens
+  // (and s = R) get the full total, written by CTA 0.
+  {
+    const int RR = R + 1;
+    const int src_real = p.T > 0 ? (int)(((int64_t)p.T + p.M - 1) / p.M) : 0;
+    const int s = b / p.blocks_per_src;
+    if (b == s * p.blocks_per_src && s < src_real)
+      for (int r = threadIdx.x; r < R; r += NT) p.psum_rs[(int64_t)r * RR + s] = bef_s[E + r];
+    if (b == 0)
+      for (int i = threadIdx.x; i < R * (RR - src_real); i += NT) {
+        const int r = i / (RR - src_real), ss = src_real + (i - r * (RR - src_real));
+        p.psum_rs[(int64_t)r * RR + ss] = tot_s[E + r];
+      }
+  }
+
   // Segment starts of the sort key (aligned expert counts, rank counts, or
   // the fixed per-expert capacity).
   const int fcap = p.fixed_cap;
@@ -281,9 +315,8 @@ __global__ void __launch_bounds__(NT) layout_assign_kernel(LayoutParams p) {
   if (b == 0) {
     // Global outputs, written once by CTA 0.  The sort key's prefix sum is
     // seg_s already; the rest is split over warps so it adds one short phase:
-    // warp 0 the other prefix sum, the error bits and the totals (then the
-    // host notification), warp 1 the padding prefix, the other warps the
-    // per-source-rank prefixes.
+    // warp 0 the error bits, the totals and the host notification, then the
+    // other prefix sum; warp 1 the padding prefix.
     for (int e = threadIdx.x; e < E; e += NT) {
       p.cnt_e[e] = tot_s[e];
       p.cnt_e_al[e] = (tot_s[e] + A - 1) / A * A;
@@ -297,67 +330,48 @@ __global__ void __launch_bounds__(NT) layout_assign_kernel(LayoutParams p) {
       for (int r = threadIdx.x; r <= R; r += NT) p.psum_r[r] = seg_s[r];
     }
     if (warp == 0) {
-      int num_expanded, num_recv;
-      bool over = false;
-      if (fcap > 0) {
-        num_expanded = warp_exclusive_scan(E, [&](int e) { return tot_s[e]; }, p.psum_e);
-        num_recv = warp_exclusive_scan(R, [&](int r) { return tot_s[E + r]; }, p.psum_r);
-        for (int e = lane; e < E; e += 32) over |= tot_s[e] > fcap;
-        over = __any_sync(0xffffffffu, over);
-      } else if (p.do_expand) {
-        num_expanded = seg_s[E];
-        num_recv = warp_exclusive_scan(R, [&](int r) { return tot_s[E + r]; }, p.psum_r);
-      } else {
-        num_recv = seg_s[R];
-        num_expanded =
-            warp_exclusive_scan(E, [&](int e) { return (tot_s[e] + A - 1) / A * A; }, p.psum_e);
-      }
+      // Totals, error bits and the host notification first (the host waits
+      // for them), the remaining prefix sums after.
       unsigned err = 0;
       for (int bb = lane; bb < p.num_blocks; bb += 32) err |= __ldcg(p.blk_err + bb);
+      int sum_r = 0, sum_e = 0, sum_al = 0;
+      bool over = false;
+      for (int r = lane; r < R; r += 32) sum_r += tot_s[E + r];
+      for (int e = lane; e < E; e += 32) {
+        sum_e += tot_s[e];
+        sum_al += (tot_s[e] + A - 1) / A * A;
+        over |= fcap > 0 && tot_s[e] > fcap;
+      }
       err = __reduce_or_sync(0xffffffffu, err);
+      const int num_recv = __reduce_add_sync(0xffffffffu, sum_r);
+      const int num_expanded = fcap > 0 ? __reduce_add_sync(0xffffffffu, sum_e)
+                                        : __reduce_add_sync(0xffffffffu, sum_al);
+      over = __any_sync(0xffffffffu, over);
       if (lane == 0) {
         const int64_t total_rows = p.do_expand ? num_expanded : num_recv;
         if (fcap > 0 ? over : total_rows > p.row_limit) err |= EP_ERRBIT_OVERFLOW;
         p.ctrl[kCtrlError] = static_cast<int>(err);
         p.ctrl[kCtrlNumRecv] = num_recv;
         p.ctrl[kCtrlNumExpanded] = num_expanded;
-        if (p.host != nullptr) {
-          p.host->error = static_cast<int>(err);
-          p.host->num_recv = num_recv;
-          p.host->num_expanded = num_expanded;
-          __threadfence_system();
-          p.host->flag = p.seq;
+        if (p.host != nullptr) {  // tagged words: no fence, the host checks each tag
+          const uint64_t tag = (uint64_t)(uint32_t)p.seq << 32;
+          p.host->num_recv = tag | (uint32_t)num_recv;
+          p.host->num_expanded = tag | (uint32_t)num_expanded;
+          p.host->error = tag | err;
         }
+      }
+      __syncwarp();
+      if (fcap > 0) {
+        warp_exclusive_scan(E, [&](int e) { return tot_s[e]; }, p.psum_e);
+        warp_exclusive_scan(R, [&](int r) { return tot_s[E + r]; }, p.psum_r);
+      } else if (p.do_expand) {
+        warp_exclusive_scan(R, [&](int r) { return tot_s[E + r]; }, p.psum_r);
+      } else {
+        warp_exclusive_scan(E, [&](int e) { return (tot_s[e] + A - 1) / A * A; }, p.psum_e);
       }
     } else if (warp == 1) {
       warp_exclusive_scan(E, [&](int e) { return (tot_s[e] + A - 1) / A * A - tot_s[e]; },
                           p.psum_pad);
-    } else {
-      // psum_rank_src[r][s]: tokens of source ranks < s received by rank r.
-      // Chunks are ordered by source rank; one warp scans each r over s.
-      const int src_ranks = p.num_blocks / p.blocks_per_src;
-      const int RR = R + 1;
-      for (int r = warp - 2; r < R; r += NWARPS - 2) {
-        int carry = 0;
-        if (lane == 0) p.psum_rs[(int64_t)r * RR] = 0;
-        for (int s0 = 0; s0 < R; s0 += 32) {
-          const int s = s0 + lane;
-          int c = 0;
-          if (s < R && s < src_ranks && p.T > 0) {
-            const int lo = s * p.blocks_per_src;
-            const int hi = min(lo + p.blocks_per_src, p.num_blocks);
-            for (int bb = lo; bb < hi; ++bb) c += __ldcg(p.blk_r + (int64_t)bb * R + r);
-          }
-          int incl = c;
-#pragma unroll
-          for (int o = 1; o < 32; o <<= 1) {
-            const int v = __shfl_up_sync(0xffffffffu, incl, o);
-            if (lane >= o) incl += v;
-          }
-          if (s < R) p.psum_rs[(int64_t)r * RR + s + 1] = carry + incl;
-          carry += __shfl_sync(0xffffffffu, incl, 31);
-        }
-      }
     }
   }
 

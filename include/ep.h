@@ -378,9 +378,10 @@ EP_API ep_status ep_validate_config(const ep_config *cfg);
 EP_API ep_status ep_upper_bound_rows(const ep_config *cfg, int64_t *rows);
 
 /*
- * The host wait used by do_cpu_sync: polls *flag until it equals `expected`
- * or `timeout_ms` passes (EP_ERR_TIMEOUT).  Exposed so the deadline logic can
- * be tested on the host with a flag that nothing sets.
+ * The host wait of do_cpu_sync in its simplest form: polls *flag until it
+ * equals `expected` or `timeout_ms` passes (EP_ERR_TIMEOUT).  (ep_layout polls
+ * three tagged words with the same loop and deadline.)  Exposed so the
+ * deadline logic can be tested on the host with a flag that nothing sets.
  */
 EP_API ep_status ep_host_wait_flag(const volatile int32_t *flag, int32_t expected,
                             int32_t timeout_ms);

@@ -247,7 +247,7 @@ cudaError_t launch_one(const CombineParams &p, int sm_cap, cudaStream_t s) {
   const int threads = consumers + 32;
   const size_t smem = (size_t)kStages * slots_cap * chunk;
   cudaError_t err;
-  if (smem > 48 * 1024) {
+  if (smem > kDynSmemOptIn) {
     err = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (err != cudaSuccess) return err;
   }

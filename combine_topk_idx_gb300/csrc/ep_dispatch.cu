@@ -408,7 +408,7 @@ cudaError_t launch_one(const DispatchParams &p0, int sm_cap, cudaStream_t s) {
   const size_t smem = kStages * (in_stage + out_stage) +
                       (FP8 && !CM ? kStages * sizeof(float) * ((H / kFp8Block + 31) / 32 * 32) : 0);
   cudaError_t err;
-  if (smem > 48 * 1024) {
+  if (smem > kDynSmemOptIn) {
     err = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (err != cudaSuccess) return err;
   }

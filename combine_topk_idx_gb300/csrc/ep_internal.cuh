@@ -111,6 +111,11 @@ struct CombineWeightsParams {
   int do_expand;
 };
 
+// Dynamic shared memory above which a kernel must opt in with
+// cudaFuncAttributeMaxDynamicSharedMemorySize: the 48 KB default window less
+// a margin for the kernels' static shared memory (all below 8 KB).
+constexpr size_t kDynSmemOptIn = 40 * 1024;
+
 // Launchers (return the first CUDA error, cudaSuccess otherwise).
 cudaError_t launch_layout(const LayoutParams &p, cudaStream_t s);
 size_t layout_assign_smem(const LayoutParams &p);

@@ -18,9 +18,9 @@
 //            holding the key in the current step).  Row = segment start +
 //            earlier chunks +
 //            earlier warps + earlier lanes, i.e. ascending (token, slot)
-//            inside every segment, with no atomics deciding positions.  CTA 0
-//            also writes the global counts and prefix sums (and, for the
-//            host count wait, the mapped totals).
+//            inside every segment, with no atomics deciding positions.  One
+//            extra CTA, which owns no chunk, writes the global counts and
+//            prefix sums (and, for the host count wait, the mapped totals).
 #include <algorithm>
 
 #include "ep_internal.cuh"
@@ -81,31 +81,6 @@ __device__ int cta_exclusive_scan(int n, F f, int32_t *out, int *warp_tot) {
   const int total = warp_tot[NWARPS];
   if (threadIdx.x == 0) out[n] = total;
   __syncthreads();
-  return total;
-}
-
-// Exclusive scan of f(i), i < n, by one warp into out[0..n]; returns the total.
-template <typename F>
-__device__ int warp_exclusive_scan(int n, F f, int32_t *out) {
-  const int lane = threadIdx.x & 31;
-  const int per = (n + 31) / 32;
-  const int beg = min(lane * per, n);
-  const int end = min(beg + per, n);
-  int local = 0;
-  for (int i = beg; i < end; ++i) local += f(i);
-  int incl = local;
-#pragma unroll
-  for (int o = 1; o < 32; o <<= 1) {
-    const int v = __shfl_up_sync(0xffffffffu, incl, o);
-    if (lane >= o) incl += v;
-  }
-  int run = incl - local;
-  for (int i = beg; i < end; ++i) {
-    out[i] = run;
-    run += f(i);
-  }
-  const int total = __shfl_sync(0xffffffffu, incl, 31);
-  if (lane == 0) out[n] = total;
   return total;
 }
 
@@ -223,10 +198,11 @@ __global__ void __launch_bounds__(NT, 1) layout_assign_kernel(LayoutParams p) {
   int *bef_s = tot_s + E + R;         // [E + R] totals of the chunks before this one
   int *seg_s = bef_s + E + R;         // [nkey + 1] segment starts
   int *rank_of = seg_s + nkey + 1;    // [E] owning rank of each expert
+  int *scan_s = rank_of + E;          // [2E + R + 1] outputs CTA: prefix sums
   // [rank_warps][nkey] 64-bit words: low half = running count of the key in
   // the warp's range, high half = lanes holding the key in the current step
   unsigned long long *whist =
-      reinterpret_cast<unsigned long long *>(rank_of + E + ((E + nkey + 1) & 1));
+      reinterpret_cast<unsigned long long *>(scan_s + 2 * E + R + 1 + ((nkey + E + R) & 1));
   __shared__ int warp_tot[NWARPS + 1];
 
   const int b = blockIdx.x;
@@ -286,68 +262,59 @@ __global__ void __launch_bounds__(NT, 1) layout_assign_kernel(LayoutParams p) {
   // psum_rank_src[r][s], the tokens of source ranks < s that rank r
   // receives, is the rank total of the chunks before source rank s's first
   // chunk: that chunk's CTA holds it in bef_s.  Source ranks without tokens
-  // (and s = R) get the full total, written by CTA 0.
+  // (and s = R) get the full total, written by the outputs CTA.
   {
     const int RR = R + 1;
     const int src_real = p.T > 0 ? (int)(((int64_t)p.T + p.M - 1) / p.M) : 0;
     const int s = b / p.blocks_per_src;
     if (b == s * p.blocks_per_src && s < src_real)
       for (int r = threadIdx.x; r < R; r += NT) p.psum_rs[(int64_t)r * RR + s] = bef_s[E + r];
-    if (b == 0)
+    if (b == p.num_blocks)
       for (int i = threadIdx.x; i < R * (RR - src_real); i += NT) {
         const int r = i / (RR - src_real), ss = src_real + (i - r * (RR - src_real));
         p.psum_rs[(int64_t)r * RR + ss] = tot_s[E + r];
       }
   }
 
-  // Segment starts of the sort key (aligned expert counts, rank counts, or
-  // the fixed per-expert capacity).
   const int fcap = p.fixed_cap;
-  if (fcap > 0) {
-    for (int e = threadIdx.x; e <= E; e += NT) seg_s[e] = e * fcap;
-    __syncthreads();
-  } else if (p.do_expand) {
-    cta_exclusive_scan(E, [&](int e) { return (tot_s[e] + A - 1) / A * A; }, seg_s, warp_tot);
-  } else {
-    cta_exclusive_scan(R, [&](int r) { return tot_s[E + r]; }, seg_s, warp_tot);
-  }
-
-  if (b == 0) {
-    // Global outputs, written once by CTA 0.  The sort key's prefix sum is
-    // seg_s already; the rest is split over warps so it adds one short phase:
-    // warp 0 the error bits, the totals and the host notification, then the
-    // other prefix sum; warp 1 the padding prefix.
-    for (int e = threadIdx.x; e < E; e += NT) {
-      p.cnt_e[e] = tot_s[e];
-      p.cnt_e_al[e] = (tot_s[e] + A - 1) / A * A;
+  if (b == p.num_blocks) {
+    // Global outputs, written once by the extra CTA that owns no chunk (so no
+    // ranking CTA waits for them).  One CTA-wide exclusive scan over
+    // [counts | aligned counts | rank counts] gives every prefix sum (read
+    // back by differences); then parallel stores, the totals and the host
+    // notification.
+    unsigned err = 0;
+    if (warp == 0)  // issued before the scan, used after it
+      for (int bb = lane; bb < p.num_blocks; bb += 32) err |= __ldcg(p.blk_err + bb);
+    cta_exclusive_scan(
+        2 * E + R,
+        [&](int i) {
+          return i < E ? tot_s[i] : i < 2 * E ? (tot_s[i - E] + A - 1) / A * A : tot_s[i - E];
+        },
+        scan_s, warp_tot);
+    const int a0 = scan_s[E], r0 = scan_s[2 * E];
+    for (int e = threadIdx.x; e <= E; e += NT) {
+      const int pc = scan_s[e], pa = scan_s[E + e] - a0;
+      if (e < E) {
+        p.cnt_e[e] = tot_s[e];
+        p.cnt_e_al[e] = (tot_s[e] + A - 1) / A * A;
+      }
+      p.psum_e[e] = fcap > 0 ? pc : pa;  // fixed capacity: the prefix of the counts
+      p.psum_pad[e] = pa - pc;
     }
-    for (int r = threadIdx.x; r < R; r += NT) p.cnt_r[r] = tot_s[E + r];
-    if (fcap > 0) {
-      // psum_expert stays the prefix of the counts (written by warp 0)
-    } else if (p.do_expand) {
-      for (int e = threadIdx.x; e <= E; e += NT) p.psum_e[e] = seg_s[e];
-    } else {
-      for (int r = threadIdx.x; r <= R; r += NT) p.psum_r[r] = seg_s[r];
+    for (int r = threadIdx.x; r <= R; r += NT) {
+      if (r < R) p.cnt_r[r] = tot_s[E + r];
+      p.psum_r[r] = scan_s[2 * E + r] - r0;
     }
     if (warp == 0) {
-      // Totals, error bits and the host notification first (the host waits
-      // for them), the remaining prefix sums after.
-      unsigned err = 0;
-      for (int bb = lane; bb < p.num_blocks; bb += 32) err |= __ldcg(p.blk_err + bb);
-      int sum_r = 0, sum_e = 0, sum_al = 0;
-      bool over = false;
-      for (int r = lane; r < R; r += 32) sum_r += tot_s[E + r];
-      for (int e = lane; e < E; e += 32) {
-        sum_e += tot_s[e];
-        sum_al += (tot_s[e] + A - 1) / A * A;
-        over |= fcap > 0 && tot_s[e] > fcap;
-      }
       err = __reduce_or_sync(0xffffffffu, err);
-      const int num_recv = __reduce_add_sync(0xffffffffu, sum_r);
-      const int num_expanded = fcap > 0 ? __reduce_add_sync(0xffffffffu, sum_e)
-                                        : __reduce_add_sync(0xffffffffu, sum_al);
+      bool over = false;
+      if (fcap > 0)
+        for (int e = lane; e < E; e += 32) over |= tot_s[e] > fcap;
       over = __any_sync(0xffffffffu, over);
       if (lane == 0) {
+        const int num_recv = scan_s[2 * E + R] - r0;
+        const int num_expanded = fcap > 0 ? a0 : r0 - a0;
         const int64_t total_rows = p.do_expand ? num_expanded : num_recv;
         if (fcap > 0 ? over : total_rows > p.row_limit) err |= EP_ERRBIT_OVERFLOW;
         p.ctrl[kCtrlError] = static_cast<int>(err);
@@ -360,24 +327,34 @@ __global__ void __launch_bounds__(NT, 1) layout_assign_kernel(LayoutParams p) {
           p.host->error = tag | err;
         }
       }
-      __syncwarp();
-      if (fcap > 0) {
-        warp_exclusive_scan(E, [&](int e) { return tot_s[e]; }, p.psum_e);
-        warp_exclusive_scan(R, [&](int r) { return tot_s[E + r]; }, p.psum_r);
-      } else if (p.do_expand) {
-        warp_exclusive_scan(R, [&](int r) { return tot_s[E + r]; }, p.psum_r);
-      } else {
-        warp_exclusive_scan(E, [&](int e) { return (tot_s[e] + A - 1) / A * A; }, p.psum_e);
-      }
-    } else if (warp == 1) {
-      warp_exclusive_scan(E, [&](int e) { return (tot_s[e] + A - 1) / A * A - tot_s[e]; },
-                          p.psum_pad);
     }
+  } else if (fcap > 0) {
+    // Segment starts of the sort key: the fixed per-expert capacity, the
+    // aligned expert counts, or the rank counts.
+    for (int e = threadIdx.x; e <= E; e += NT) seg_s[e] = e * fcap;
+    __syncthreads();
+  } else if (p.do_expand) {
+    cta_exclusive_scan(E, [&](int e) { return (tot_s[e] + A - 1) / A * A; }, seg_s, warp_tot);
+  } else {
+    cta_exclusive_scan(R, [&](int r) { return tot_s[E + r]; }, seg_s, warp_tot);
   }
+  if (b == p.num_blocks) return;  // the outputs CTA ranks nothing
 
-  // Sort key per slot: the expert (expanded) or, for the lowest slot of the
-  // token on each rank, the rank (rank layout).
-  for (int i = threadIdx.x; i < ns; i += NT) {
+  // Stable ranking: rank warp w owns the contiguous slot range [beg, end).
+  // Pass 1 computes each slot's sort key -- the expert (expanded) or, for
+  // the lowest slot of the token on each rank, the rank (rank layout) -- and
+  // counts keys per warp (shared-memory atomics, order-free); after the
+  // bases are known, pass 2 walks the range in order, 32 slots a step: every
+  // lane ORs its bit into its key's word, the word then names the lanes
+  // sharing the key (their order = slot order), and the lowest of them
+  // advances the key's running count.  A word is two 32-bit halves (count,
+  // lane mask), so both updates are 32-bit shared atomics and one 64-bit
+  // load reads both.
+  const int per_warp = (ns + nrw - 1) / nrw;
+  const int beg = min(warp * per_warp, ns);
+  const int end = warp < nrw ? min(beg + per_warp, ns) : beg;
+  unsigned long long *wh = whist + (size_t)warp * nkey;
+  for (int i = beg + lane; i < end; i += 32) {
     const int e = idx_s[i];
     int key = -1;
     if (e >= 0) {
@@ -395,22 +372,7 @@ __global__ void __launch_bounds__(NT, 1) layout_assign_kernel(LayoutParams p) {
       }
     }
     row_s[i] = key;
-  }
-  __syncthreads();
-
-  // Stable ranking: rank warp w owns the contiguous slot range [beg, end).
-  // Pass 1 counts keys per warp (shared-memory atomics, order-free); after
-  // the bases are known, pass 2 walks the range in order, 32 slots a step:
-  // every lane ORs its bit into its key's word, the word then names the
-  // lanes sharing the key (their order = slot order), and the lowest of them
-  // advances the key's running count.
-  const int per_warp = (ns + nrw - 1) / nrw;
-  const int beg = min(warp * per_warp, ns);
-  const int end = warp < nrw ? min(beg + per_warp, ns) : beg;
-  unsigned long long *wh = whist + (size_t)warp * nkey;
-  for (int i = beg + lane; i < end; i += 32) {
-    const int key = row_s[i];
-    if (key >= 0) atomicAdd(&wh[key], 1ull);
+    if (key >= 0) atomicAdd(reinterpret_cast<unsigned *>(&wh[key]), 1u);
   }
   __syncthreads();
   const int boff = p.do_expand ? 0 : E;
@@ -423,11 +385,14 @@ __global__ void __launch_bounds__(NT, 1) layout_assign_kernel(LayoutParams p) {
     }
   }
   __syncthreads();
+  // Expanded layout: every slot owns its row, so pass 2 writes dst and the
+  // row metadata directly; the rank layout resolves shared rows afterwards.
+  int2 *meta = reinterpret_cast<int2 *>(p.meta);
   const unsigned lt = (1u << lane) - 1u;
   for (int s0 = beg; s0 < end; s0 += 32) {
     const int i = s0 + lane;
     const int key = i < end ? row_s[i] : -1;
-    if (key >= 0) atomicOr(&wh[key], 1ull << (32 + lane));
+    if (key >= 0) atomicOr(reinterpret_cast<unsigned *>(&wh[key]) + 1, 1u << lane);
     __syncwarp();
     const unsigned long long word = key >= 0 ? wh[key] : 0ull;
     const unsigned peers = (unsigned)(word >> 32);
@@ -437,41 +402,47 @@ __global__ void __launch_bounds__(NT, 1) layout_assign_kernel(LayoutParams p) {
     if (key >= 0 && lane == __ffs(peers) - 1)
       wh[key] = (unsigned long long)((unsigned)word + __popc(peers));
     __syncwarp();
-    if (i < end) row_s[i] = row;
-  }
-  __syncthreads();
-
-  int2 *meta = reinterpret_cast<int2 *>(p.meta);
-  for (int i = threadIdx.x; i < ns; i += NT) {
-    const int tl = i / K, k = i - tl * K;
-    const int own = row_s[i];
-    int row = own;
-    const int e = idx_s[i];
-    if (!p.do_expand && e >= 0 && own < 0) {
-      // another (lower) slot of this token on the same rank owns the row
-      const int r = rank_of[e];
-      for (int j = 0; j < k; ++j) {
-        const int f = idx_s[tl * K + j];
-        if (f >= 0 && rank_of[f] == r) {
-          row = row_s[tl * K + j];
-          break;
-        }
+    if (i < end) {
+      if (p.do_expand) {
+        bool keep = row >= 0 && row < p.row_limit;
+        if (fcap > 0 && row >= 0 && row >= (key + 1) * fcap) keep = false;  // past capacity
+        p.dst[base + i] = keep ? row : -1;
+        if (keep) meta[row] = make_int2(t0 + i / K, i % K);
+      } else {
+        row_s[i] = row;
       }
     }
-    bool keep = own >= 0 && own < p.row_limit;
-    if (fcap > 0 && own >= 0 && own >= (e + 1) * fcap) {  // past the expert's capacity
-      row = -1;
-      keep = false;
-    }
-    if (row >= p.row_limit) row = -1;
-    p.dst[base + i] = row;
-    if (keep) meta[own] = make_int2(t0 + tl, k);
   }
 
-  if (p.do_expand && fcap == 0) {
+  if (!p.do_expand) {
+    __syncthreads();
+    for (int i = threadIdx.x; i < ns; i += NT) {
+      const int tl = i / K, k = i - tl * K;
+      const int own = row_s[i];
+      int row = own;
+      const int e = idx_s[i];
+      if (e >= 0 && own < 0) {
+        // another (lower) slot of this token on the same rank owns the row
+        const int r = rank_of[e];
+        for (int j = 0; j < k; ++j) {
+          const int f = idx_s[tl * K + j];
+          if (f >= 0 && rank_of[f] == r) {
+            row = row_s[tl * K + j];
+            break;
+          }
+        }
+      }
+      if (row >= p.row_limit) row = -1;
+      p.dst[base + i] = row;
+      if (own >= 0 && own < p.row_limit) meta[own] = make_int2(t0 + tl, k);
+    }
+  }
+
+  if (p.do_expand && fcap == 0 && b < p.num_blocks) {
     // alignment padding rows -> (-1, -1): one warp per expert, experts
-    // b + (warp + NWARPS * i) * gridDim.x
-    for (int e = b + warp * (int)gridDim.x; e < E; e += NWARPS * (int)gridDim.x) {
+    // b + (warp + NWARPS * i) * num_blocks over the ranking CTAs (the outputs
+    // CTA has no segment starts)
+    for (int e = b + warp * p.num_blocks; e < E; e += NWARPS * p.num_blocks) {
       const int64_t r0 = (int64_t)seg_s[e] + tot_s[e];
       const int64_t r1 = min((int64_t)seg_s[e + 1], p.row_limit);
       for (int64_t r = r0 + lane; r < r1; r += 32) meta[r] = make_int2(-1, -1);
@@ -484,7 +455,7 @@ __global__ void __launch_bounds__(NT, 1) layout_assign_kernel(LayoutParams p) {
 size_t layout_assign_smem(const LayoutParams &p) {
   const int nkey = p.do_expand ? p.E : p.R;
   return sizeof(int) * (2 * (size_t)p.chunk_tokens * p.K + 2 * (size_t)(p.E + p.R) + nkey + 1 +
-                        p.E + 1) +
+                        p.E + 2 * (size_t)p.E + p.R + 1 + 1) +
          sizeof(unsigned long long) * (size_t)p.rank_warps * nkey;
 }
 
@@ -500,12 +471,12 @@ cudaError_t launch_layout(const LayoutParams &p, cudaStream_t s) {
   const size_t smem_count = sizeof(int) * (2 * (size_t)p.E + p.R + (size_t)p.chunk_tokens * p.K);
   const size_t smem_assign = layout_assign_smem(p);
   cudaError_t err;
-  if (smem_count > 48 * 1024) {
+  if (smem_count > kDynSmemOptIn) {
     err = cudaFuncSetAttribute(layout_count_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                (int)smem_count);
     if (err != cudaSuccess) return err;
   }
-  if (smem_assign > 48 * 1024) {
+  if (smem_assign > kDynSmemOptIn) {
     err = cudaFuncSetAttribute(layout_assign_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                (int)smem_assign);
     if (err != cudaSuccess) return err;
@@ -516,7 +487,7 @@ cudaError_t launch_layout(const LayoutParams &p, cudaStream_t s) {
   // assign may launch while count drains (programmatic dependent launch); it
   // waits on griddepcontrol before touching count's outputs
   cudaLaunchConfig_t lc{};
-  lc.gridDim = dim3(p.num_blocks);
+  lc.gridDim = dim3(p.num_blocks + 1);  // + the outputs CTA
   lc.blockDim = dim3(NT);
   lc.dynamicSmemBytes = smem_assign;
   lc.stream = s;

@@ -395,3 +395,20 @@ def test_cuda_graph_capture_and_replay(ep, name, T):
         assert torch.equal(got["recv_topk_weights"][:total], eager["recv_topk_weights"][:total])
         assert torch.equal(got_res, ref)
         h.free()
+
+
+def test_shared_memory_window_edges(ep):
+    """Shapes whose dynamic shared memory is exactly the 48 KB default window
+    (which the kernels' static shared memory pushes past): the combine with a
+    per-expert bias at hidden 7168 and top-8, and the BF16 dispatch at hidden
+    8192."""
+    T, K, E, R, H, M = 64, 8, 16, 4, 7168, 16
+    idx, w = _routing(T, K, E, seed=21)
+    x = torch.randn(T, H, generator=torch.Generator().manual_seed(2)).to(torch.bfloat16)
+    eb = W.hashed_bf16_rows(torch.arange(E), H, 17)
+    run_and_check(ep, ep.make_config(T, K, E, R, H, M, 4, True, True, True),
+                  idx, x, w, expert_bias=eb)
+    T, K, E, R, H, M = 48, 2, 8, 2, 8192, 24
+    idx, w = _routing(T, K, E, seed=22)
+    x = torch.randn(T, H, generator=torch.Generator().manual_seed(3)).to(torch.bfloat16)
+    run_and_check(ep, ep.make_config(T, K, E, R, H, M, 1, False, False, True), idx, x, w)

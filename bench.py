@@ -424,23 +424,29 @@ def run_gpu(args, ws, rank, local):
 
     # e2e through the C ABI with host buffers: every step copies its inputs
     # (topk_idx, topk_weights, x) in from pinned host memory and its combined
-    # output back out.  Consecutive steps alternate between two streams and
-    # two buffer sets, so one step's copies overlap the neighbouring steps'
-    # kernels, as a serving loop would run them.
+    # output back out.  Steps rotate over three streams and buffer sets, and
+    # the next step's input copies are enqueued before this step's layout
+    # (whose count wait blocks the host), so one step's copies overlap the
+    # neighbouring steps' kernels and copies, as a serving loop would run them.
     idx_pin, w_pin, x_pin = idx_h.pin_memory(), w_h.pin_memory(), x_h.pin_memory()
-    e2e_streams = [torch.cuda.Stream(device=dev), torch.cuda.Stream(device=dev)]
+    nbuf = 3
+    e2e_streams = [torch.cuda.Stream(device=dev) for _ in range(nbuf)]
     e2e_bufs = [{"idx": torch.empty_like(idx), "w": torch.empty_like(w), "x": torch.empty_like(x),
                  "out": torch.empty((T, H), dtype=torch.bfloat16, device=dev),
                  "out_pin": torch.empty((T, H), dtype=torch.bfloat16).pin_memory()}
-                for _ in range(2)]
+                for _ in range(nbuf)]
 
-    def e2e_step(i):
-        st = e2e_streams[i % 2]
-        b = e2e_bufs[i % 2]
-        with torch.cuda.stream(st):
+    def e2e_copy_in(i):
+        b = e2e_bufs[i % nbuf]
+        with torch.cuda.stream(e2e_streams[i % nbuf]):
             b["idx"].copy_(idx_pin, non_blocking=True)
             b["w"].copy_(w_pin, non_blocking=True)
             b["x"].copy_(x_pin, non_blocking=True)
+
+    def e2e_step(i):
+        st = e2e_streams[i % nbuf]
+        b = e2e_bufs[i % nbuf]
+        with torch.cuda.stream(st):
             h = ep.ep_layout(cfg, b["idx"], stream=st)
             out = ep.alloc_recv(h, with_weights=True, with_idx=True)
             ep.ep_dispatch(h, b["x"], b["w"], **out, stream=st)
@@ -451,7 +457,10 @@ def run_gpu(args, ws, rank, local):
     def e2e_run(n):
         for st in e2e_streams:
             st.wait_stream(stream)
+        e2e_copy_in(0)
         for i in range(n):
+            if i + 1 < n:
+                e2e_copy_in(i + 1)
             e2e_step(i)
         for st in e2e_streams:
             stream.wait_stream(st)
@@ -583,7 +592,8 @@ def run_gpu(args, ws, rank, local):
                 "ms_per_step": round(e2e_ms, 5),
                 "how": "C ABI with host buffers: per step, pinned h2d of topk_idx, weights and x, "
                        "layout + dispatch + combine, d2h of the output; consecutive steps "
-                       "alternate two streams (copies overlap neighbouring steps)",
+                       "rotate over three streams, the next step's inputs are copied in before "
+                       "this step's layout (copies overlap neighbouring steps)",
                 "h2d_bytes_per_step": idx_h.numel() * 8 + w_h.numel() * 4 + x_h.numel() * 2,
                 "d2h_bytes_per_step": T * H * 2},
         "gpu_launches": launches,

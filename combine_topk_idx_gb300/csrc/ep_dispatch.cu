@@ -40,6 +40,7 @@ constexpr int kMaxConsumers = 224;
 constexpr int kWaitIters = 4000;          // x kWaitHintNs: gives up after ~2 s
 constexpr uint32_t kWaitHintNs = 500000;
 constexpr int kBarConsumers = 1;          // named barrier id (0 is __syncthreads)
+constexpr int kSfRowsPerThread = 4;       // scale gather: rows per thread
 
 // What the kernel does with a source row.
 constexpr int kModeBf16 = 0;    // BF16 in, BF16 copy out
@@ -357,11 +358,12 @@ __device__ __forceinline__ void sf_expand_one(const DispatchParams &p, int nb, i
     if (j0 + u < nb) dst[(int64_t)u * p.sf_hidden_stride] = v[u];
 }
 
+template <bool FIXED>
 __global__ void __launch_bounds__(256) sf_expand_kernel(DispatchParams p) {
   griddep_wait();  // the per-token scales come from the dispatch kernel
   const int nb = p.H / kFp8Block;
   const int2 *meta = reinterpret_cast<const int2 *>(p.meta);
-  if (p.fixed_cap > 0) {
+  if constexpr (FIXED) {
     // grid (x, 1, E): the CTAs of expert e walk its used rows i < count,
     // group of 4 scale blocks by group, consecutive threads on consecutive
     // rows of one group (coalesced stores into the expert's column-major slab)
@@ -377,15 +379,27 @@ __global__ void __launch_bounds__(256) sf_expand_kernel(DispatchParams p) {
       sf_expand_one(p, nb, j0, __ldg(&meta[row0 + i].x),
                     out0 + i + (int64_t)j0 * p.sf_hidden_stride);
     }
-    return;
+  } else {
+    // one global column-major matrix over the rows below the layout's total:
+    // grid (blocks of kSfRowsPerThread * 256 rows, groups of 4 scale blocks);
+    // a thread takes rows r, r + 256, ... so each step of a warp stays
+    // coalesced, and its kSfRowsPerThread metadata loads are all in flight
+    const int64_t n = min((int64_t)__ldg(p.num_rows), p.rows_alloc);
+    const int64_t row0 = (int64_t)blockIdx.x * blockDim.x * kSfRowsPerThread + threadIdx.x;
+    const int j0 = blockIdx.y * 4;
+    int tok[kSfRowsPerThread];
+#pragma unroll
+    for (int u = 0; u < kSfRowsPerThread; ++u) {
+      const int64_t row = row0 + (int64_t)u * blockDim.x;
+      tok[u] = row < n ? __ldg(&meta[row].x) : -2;
+    }
+#pragma unroll
+    for (int u = 0; u < kSfRowsPerThread; ++u) {
+      const int64_t row = row0 + (int64_t)u * blockDim.x;
+      if (tok[u] != -2)
+        sf_expand_one(p, nb, j0, tok[u], p.recv_sf + row + (int64_t)j0 * p.sf_hidden_stride);
+    }
   }
-  // one global column-major matrix over the rows below the layout's total:
-  // grid (row blocks, groups of 4 scale blocks)
-  const int64_t n = min((int64_t)__ldg(p.num_rows), p.rows_alloc);
-  const int64_t row = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
-  if (row >= n) return;
-  const int j0 = blockIdx.y * 4;
-  sf_expand_one(p, nb, j0, __ldg(&meta[row].x), p.recv_sf + row + (int64_t)j0 * p.sf_hidden_stride);
 }
 
 template <int MODE, bool CM>
@@ -436,7 +450,8 @@ cudaError_t launch_one(const DispatchParams &p0, int sm_cap, cudaStream_t s) {
     sf_grid = dim3((unsigned)std::min<int64_t>(4, ((int64_t)p.fixed_cap * groups + 2047) / 2048), 1,
                    (unsigned)p.E);
   else
-    sf_grid = dim3((unsigned)((p.rows_alloc + 255) / 256), (unsigned)groups);
+    sf_grid = dim3((unsigned)((p.rows_alloc + 256 * kSfRowsPerThread - 1) / (256 * kSfRowsPerThread)),
+                   (unsigned)groups);
   if (p.rows_alloc > 0) {
     // launched while the dispatch kernel drains; it waits on griddepcontrol
     cudaLaunchConfig_t lc{};
@@ -448,7 +463,8 @@ cudaError_t launch_one(const DispatchParams &p0, int sm_cap, cudaStream_t s) {
     attr[0].val.programmaticStreamSerializationAllowed = 1;
     lc.attrs = attr;
     lc.numAttrs = 1;
-    err = cudaLaunchKernelEx(&lc, sf_expand_kernel, p);
+    err = p.fixed_cap > 0 ? cudaLaunchKernelEx(&lc, sf_expand_kernel<true>, p)
+                         : cudaLaunchKernelEx(&lc, sf_expand_kernel<false>, p);
   }
   return err;
 }

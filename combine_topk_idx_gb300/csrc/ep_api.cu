@@ -207,6 +207,7 @@ DispatchParams dispatch_params(const ep_handle *h, const void *x, const float *t
   p.sf_src_hs = 1;
   p.fixed_cap = h->lp.fixed_cap;
   p.sf_expert_stride = h->sf_expert_stride;
+  p.sf_sync = h->lp.disp_sync;
   return p;
 }
 
@@ -351,6 +352,7 @@ ep_status ep_layout(const ep_config *cfg, const void *topk_idx, ep_stream_t stre
     return o;
   };
   const size_t o_ctrl = take(sizeof(int32_t) * ep::kCtrlWords);
+  const size_t o_sync = take(sizeof(int32_t) * 2);
   const size_t o_topk = take(sizeof(int32_t) * (size_t)T * K);
   const size_t o_dst = take(sizeof(int32_t) * (size_t)T * K);
   const size_t o_meta = take(sizeof(int32_t) * 2 * (size_t)lp.row_limit);
@@ -379,6 +381,7 @@ ep_status ep_layout(const ep_config *cfg, const void *topk_idx, ep_stream_t stre
   if (ce != cudaSuccess) return ep::cuda_status(ce);
   uint8_t *base = static_cast<uint8_t *>(dmem);
   lp.ctrl = reinterpret_cast<int32_t *>(base + o_ctrl);
+  lp.disp_sync = reinterpret_cast<int32_t *>(base + o_sync);
   lp.topk32 = reinterpret_cast<int32_t *>(base + o_topk);
   lp.dst = reinterpret_cast<int32_t *>(base + o_dst);
   lp.meta = reinterpret_cast<int32_t *>(base + o_meta);

@@ -7,10 +7,10 @@
 //
 // Token-major scatter with persistent, warp-specialised CTAs:
 //   warp 0 (producer) takes the CTA's tokens in turn, reads each token's K
-//     destination rows (prefetched one token ahead), keeps the distinct ones
+//     destination rows (prefetched four tokens ahead), keeps the distinct ones
 //     (rank-layout slots of one rank share a row), writes the per-row weights
 //     and local expert ids, and issues one cp.async.bulk global->shared copy
-//     of the token's BF16 row into a ring of kStages input stages;
+//     of the token's source row into a ring of kStages input stages;
 //   the consumer warps wait for a stage and
 //     FP8:  quantise it -- amax of each 128-element block by a 16-lane
 //           shuffle, scale = amax / 448 and x / scale with IEEE divisions,
@@ -41,6 +41,11 @@ constexpr int kWaitIters = 4000;          // x kWaitHintNs: gives up after ~2 s
 constexpr uint32_t kWaitHintNs = 500000;
 constexpr int kBarConsumers = 1;          // named barrier id (0 is __syncthreads)
 constexpr int kSfRowsPerThread = 4;       // scale gather: rows per thread
+constexpr int kSfWaitIters = 8000000;     // x ~256 ns: the gather gives up after ~2 s
+// What the scale gather waits for before reading per-token scales.
+constexpr int kSfWaitNone = 0;            // nothing: the caller's scales (pre-quantised)
+constexpr int kSfWaitHandshake = 1;       // every dispatch CTA's published counter
+constexpr int kSfWaitGrid = 2;            // the whole dispatch grid (griddepcontrol.wait)
 
 // What the kernel does with a source row.
 constexpr int kModeBf16 = 0;    // BF16 in, BF16 copy out
@@ -227,8 +232,24 @@ __global__ void __launch_bounds__(kMaxConsumers + 32, 1) dispatch_kernel(Dispatc
   uint8_t *recv = static_cast<uint8_t *>(p.recv_x);
   int64_t i = 0;
   int pi = 0;
+  // Once the CTA's tokens are done (every token item comes before the padding
+  // items): publish that their per-token scales are written, and let the
+  // scale gather launch.  Uniform over the consumer threads.
+  bool signalled = false;
+  auto tokens_done = [&]() {
+    if constexpr (FP8 && COL_MAJOR) {
+      if (p.sf_wait == kSfWaitHandshake) {
+        __threadfence();
+        named_barrier(kBarConsumers, nct);
+        if (ctid == 0) atomicAdd(p.sf_sync, 1);
+      }
+    }
+    griddep_launch_dependents();
+    signalled = true;
+  };
   for (int64_t item = blockIdx.x; item < num_items; item += gridDim.x) {
-    if (item >= p.T) {  // every token item comes before the padding items
+    if (item >= p.T) {
+      if (!signalled) tokens_done();
       zero_padding_item(p, (int)(item - p.T), npad, prow_s[pi & 1], FP8_OUT, COL_MAJOR, ctid, nct);
       ++pi;
       continue;
@@ -330,7 +351,7 @@ __global__ void __launch_bounds__(kMaxConsumers + 32, 1) dispatch_kernel(Dispatc
       if (lane == 0) mbar_arrive(&empty[s]);
     }
   }
-  griddep_launch_dependents();
+  if (!signalled) tokens_done();
   if (ctid == 0) bulk_wait_all<0>();
 }
 
@@ -345,12 +366,16 @@ __device__ __forceinline__ void sf_expand_one(const DispatchParams &p, int nb, i
                                               float *dst) {
   float v[4] = {0.f, 0.f, 0.f, 0.f};
   if (tok >= 0) {
+    // scales written by the running dispatch kernel are read through L2 only
     const float *src = p.sf_src + (int64_t)tok * p.sf_src_ts + (int64_t)j0 * p.sf_src_hs;
     if (p.sf_src_vec4) {
-      const float4 q = __ldg(reinterpret_cast<const float4 *>(src));
+      const float4 q = p.sf_wait == kSfWaitHandshake ? __ldcg(reinterpret_cast<const float4 *>(src))
+                                 : __ldg(reinterpret_cast<const float4 *>(src));
       v[0] = q.x; v[1] = q.y; v[2] = q.z; v[3] = q.w;
     } else {
-      for (int u = 0; u < 4 && j0 + u < nb; ++u) v[u] = __ldg(src + (int64_t)u * p.sf_src_hs);
+      for (int u = 0; u < 4 && j0 + u < nb; ++u)
+        v[u] = p.sf_wait == kSfWaitHandshake ? __ldcg(src + (int64_t)u * p.sf_src_hs)
+                         : __ldg(src + (int64_t)u * p.sf_src_hs);
     }
   }
 #pragma unroll
@@ -359,8 +384,7 @@ __device__ __forceinline__ void sf_expand_one(const DispatchParams &p, int nb, i
 }
 
 template <bool FIXED>
-__global__ void __launch_bounds__(256) sf_expand_kernel(DispatchParams p) {
-  griddep_wait();  // the per-token scales come from the dispatch kernel
+__device__ __forceinline__ void sf_expand_body(const DispatchParams &p) {
   const int nb = p.H / kFp8Block;
   const int2 *meta = reinterpret_cast<const int2 *>(p.meta);
   if constexpr (FIXED) {
@@ -402,6 +426,40 @@ __global__ void __launch_bounds__(256) sf_expand_kernel(DispatchParams p) {
   }
 }
 
+template <bool FIXED>
+__global__ void __launch_bounds__(256) sf_expand_kernel(DispatchParams p) {
+  // Launched while the dispatch kernel still runs (programmatic dependent
+  // launch).  With sf_wait the per-token scales come from that kernel: wait,
+  // bounded, until every dispatch CTA has published its tokens' scales.
+  if (p.sf_wait == kSfWaitGrid) griddep_wait();
+  __shared__ int ready;
+  if (threadIdx.x == 0) {
+    bool ok = true;
+    if (p.sf_wait == kSfWaitHandshake) {
+      ok = false;
+      for (int it = 0; it < kSfWaitIters && !ok; ++it) {
+        ok = ld_acquire_gpu(p.sf_sync) >= p.sf_sync_target;
+        if (!ok) __nanosleep(256);
+      }
+      if (!ok) atomicOr(p.err, EP_ERRBIT_TIMEOUT);
+    }
+    ready = ok;
+  }
+  __syncthreads();
+  if (ready) sf_expand_body<FIXED>(p);
+  if (p.sf_wait == kSfWaitHandshake) {
+    // the last CTA resets the handshake for the next dispatch on this handle
+    __syncthreads();
+    if (threadIdx.x == 0) {
+      const int total = (int)(gridDim.x * gridDim.y * gridDim.z);
+      if (atomicAdd(p.sf_sync + 1, 1) == total - 1) {
+        p.sf_sync[0] = 0;
+        p.sf_sync[1] = 0;
+      }
+    }
+  }
+}
+
 template <int MODE, bool CM>
 cudaError_t launch_one(const DispatchParams &p0, int sm_cap, cudaStream_t s) {
   constexpr bool FP8 = MODE == kModeQuant;
@@ -438,6 +496,12 @@ cudaError_t launch_one(const DispatchParams &p0, int sm_cap, cudaStream_t s) {
   const int64_t items = (int64_t)p.T + p.max_pad_items;
   const int64_t grid = std::min<int64_t>((int64_t)use_sms * per_sm, items);
   if (grid <= 0) return cudaSuccess;
+  p.sf_sync_target = (int)grid;        // every dispatch CTA publishes once
+  // quantising: the gather needs the kernel's scales -- by the handshake, or
+  // (fixed capacity: few rows per expert) after the whole kernel
+  p.sf_wait = MODE != kModeQuant ? kSfWaitNone
+              : p.fixed_cap > 0  ? kSfWaitGrid
+                                 : kSfWaitHandshake;
   kern<<<(int)grid, threads, smem, s>>>(p);
   err = cudaGetLastError();
   if (err != cudaSuccess || MODE == kModeBf16 || !CM) return err;
@@ -453,7 +517,7 @@ cudaError_t launch_one(const DispatchParams &p0, int sm_cap, cudaStream_t s) {
     sf_grid = dim3((unsigned)((p.rows_alloc + 256 * kSfRowsPerThread - 1) / (256 * kSfRowsPerThread)),
                    (unsigned)groups);
   if (p.rows_alloc > 0) {
-    // launched while the dispatch kernel drains; it waits on griddepcontrol
+    // launched as soon as every dispatch CTA is past its tokens
     cudaLaunchConfig_t lc{};
     lc.gridDim = sf_grid;
     lc.blockDim = dim3(256);

@@ -34,6 +34,8 @@ struct LayoutParams {
   int T, K, E, R, L, M, A;
   int do_expand;
   int fixed_cap;          // > 0: fixed-capacity layout, rows per expert (do_expand only)
+  int32_t *disp_sync;     // [2] handle only (else nullptr): dispatch / scale-gather
+                          // handshake counters, zeroed by the layout
   int num_blocks;         // layout grid (one CTA per chunk of tokens)
   int blocks_per_src;     // chunks per source rank
   int chunk_tokens;       // tokens per chunk
@@ -88,6 +90,14 @@ struct DispatchParams {
   // between experts' column-major slabs
   int fixed_cap;
   int64_t sf_expert_stride;
+  // Quantising dispatch with column-major scales: every dispatch CTA adds 1 to
+  // sf_sync[0] once its tokens' scales are written; the scale gather, launched
+  // early, waits (bounded) for sf_sync_target and its last CTA resets both
+  // counters.  sf_wait selects what the gather waits for (none / this
+  // handshake / the whole dispatch grid).
+  int32_t *sf_sync;
+  int sf_sync_target;
+  int sf_wait;
 };
 
 struct CombineParams {

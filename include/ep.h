@@ -195,7 +195,9 @@ EP_API ep_status ep_layout(const ep_config *cfg, const void *topk_idx, ep_stream
  * Padding rows (expanded) get weight 0; with do_zero_padding also zero
  *   payload and zero scales.  Rows past the real total are not written.
  * Must be ordered after ep_layout of the same handle (same stream, or the
- *   caller's own event).  May be called again with new x (cached dispatch).
+ *   caller's own event).  May be called again with new x (cached dispatch);
+ *   dispatches on one handle must not overlap on the GPU (they share the
+ *   handle's scale-gather handshake words).
  */
 EP_API ep_status ep_dispatch(ep_handle *h, const void *x, const float *topk_weights,
                       void *recv_x, float *recv_sf, float *recv_topk_weights,

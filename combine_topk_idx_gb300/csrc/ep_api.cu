@@ -208,6 +208,7 @@ DispatchParams dispatch_params(const ep_handle *h, const void *x, const float *t
   p.fixed_cap = h->lp.fixed_cap;
   p.sf_expert_stride = h->sf_expert_stride;
   p.sf_sync = h->lp.disp_sync;
+  p.sched = h->lp.disp_sync + 2;
   return p;
 }
 
@@ -352,7 +353,7 @@ ep_status ep_layout(const ep_config *cfg, const void *topk_idx, ep_stream_t stre
     return o;
   };
   const size_t o_ctrl = take(sizeof(int32_t) * ep::kCtrlWords);
-  const size_t o_sync = take(sizeof(int32_t) * 2);
+  const size_t o_sync = take(sizeof(int32_t) * ep::kDispSyncWords);
   const size_t o_topk = take(sizeof(int32_t) * (size_t)T * K);
   const size_t o_dst = take(sizeof(int32_t) * (size_t)T * K);
   const size_t o_meta = take(sizeof(int32_t) * 2 * (size_t)lp.row_limit);

@@ -55,6 +55,7 @@ constexpr int kModePreq = 2;    // e4m3 + fp32 scales in, copied
 struct TokenMeta {
   int rows[EP_MAX_TOPK];
   int n;
+  int t;  // source token, or -1: no more tokens for this CTA
 };
 
 // Expert whose padding range holds padding row q: the last e with psum_pad[e] <= q.
@@ -159,20 +160,17 @@ __global__ void __launch_bounds__(kMaxConsumers + 32, 1) dispatch_kernel(Dispatc
   const uint64_t stream_pol = l2_policy_evict_first();
   if (warp == 0) {
     // ---------------- producer ----------------
-    // routing of the next kPrefetch tokens is in flight while one is issued
-    int t = blockIdx.x;
+    // The first token of each CTA is its index; the rest are handed out
+    // dynamically from a handle counter, so CTAs that run faster take more of
+    // them.  The next token and its routing are fetched while the current
+    // one is issued.
     const int G = gridDim.x;
-    Routing r0{-1, -1, 0.f}, r1{-1, -1, 0.f}, r2{-1, -1, 0.f}, r3{-1, -1, 0.f};
-    if (t < p.T) r0 = load_routing(p, t, lane);
-    if (t + G < p.T) r1 = load_routing(p, t + G, lane);
-    if (t + 2 * G < p.T) r2 = load_routing(p, t + 2 * G, lane);
-    if (t + 3 * G < p.T) r3 = load_routing(p, t + 3 * G, lane);
-    for (int64_t i = 0; t < p.T; ++i, t += G) {
-      const Routing cur = r0;
-      r0 = r1;
-      r1 = r2;
-      r2 = r3;
-      if (t + 4 * (int64_t)G < p.T) r3 = load_routing(p, t + 4 * G, lane);
+    int next = blockIdx.x;
+    Routing rn{-1, -1, 0.f};
+    if (next < p.T) rn = load_routing(p, next, lane);
+    for (int64_t i = 0;; ++i) {
+      const int t = next;
+      const Routing cur = rn;
       const int s = (int)(i % kStages);
       const int64_t k = i / kStages;
       if (k > 0) {
@@ -185,12 +183,25 @@ __global__ void __launch_bounds__(kMaxConsumers + 32, 1) dispatch_kernel(Dispatc
           return;
         }
       }
+      if (t >= p.T) {  // end marker for the consumers
+        if (lane == 0) {
+          meta[s].t = -1;
+          mbar_arrive(&full[s]);
+        }
+        break;
+      }
+      if (lane == 0) next = G + atomicAdd(p.sched, 1);
+      next = __shfl_sync(0xffffffffu, next, 0);
+      if (next < p.T) rn = load_routing(p, next, lane);
       const unsigned peers = __match_any_sync(0xffffffffu, cur.d);
       const bool keep = cur.d >= 0 && lane == __ffs(peers) - 1;
       const unsigned keepm = __ballot_sync(0xffffffffu, keep);
       const int n = __popc(keepm);
       if (keep) meta[s].rows[__popc(keepm & lanemask_lt())] = cur.d;
-      if (lane == 0) meta[s].n = n;
+      if (lane == 0) {
+        meta[s].n = n;
+        meta[s].t = t;
+      }
       if (p.do_expand) {
         if (keep && p.recv_w != nullptr) p.recv_w[cur.d] = cur.w;
       } else if (p.recv_w != nullptr || p.recv_idx != nullptr) {
@@ -228,42 +239,19 @@ __global__ void __launch_bounds__(kMaxConsumers + 32, 1) dispatch_kernel(Dispatc
   const int nvec = H / 8;  // 16-byte vectors of the BF16 row
   const bool pad_work = p.do_expand && (p.zero_padding || p.recv_w != nullptr);
   const int npad = pad_work ? __ldg(p.psum_pad + p.E) : 0;
-  const int64_t num_items = (int64_t)p.T + (npad + kPadRowsPerItem - 1) / kPadRowsPerItem;
+  const int64_t pad_items = (npad + kPadRowsPerItem - 1) / kPadRowsPerItem;
   uint8_t *recv = static_cast<uint8_t *>(p.recv_x);
-  int64_t i = 0;
-  int pi = 0;
-  // Once the CTA's tokens are done (every token item comes before the padding
-  // items): publish that their per-token scales are written, and let the
-  // scale gather launch.  Uniform over the consumer threads.
-  bool signalled = false;
-  auto tokens_done = [&]() {
-    if constexpr (FP8 && COL_MAJOR) {
-      if (p.sf_wait == kSfWaitHandshake) {
-        __threadfence();
-        named_barrier(kBarConsumers, nct);
-        if (ctid == 0) atomicAdd(p.sf_sync, 1);
-      }
-    }
-    griddep_launch_dependents();
-    signalled = true;
-  };
-  for (int64_t item = blockIdx.x; item < num_items; item += gridDim.x) {
-    if (item >= p.T) {
-      if (!signalled) tokens_done();
-      zero_padding_item(p, (int)(item - p.T), npad, prow_s[pi & 1], FP8_OUT, COL_MAJOR, ctid, nct);
-      ++pi;
-      continue;
-    }
+  for (int64_t i = 0;; ++i) {
     const int s = (int)(i % kStages);
     const uint32_t par = (uint32_t)((i / kStages) & 1);
-    ++i;
     if (!mbar_wait_bounded(&full[s], par, kWaitIters, kWaitHintNs)) {
       if (lane == 0) atomicOr(p.err, EP_ERRBIT_TIMEOUT);
       if (ctid == 0) bulk_wait_all<0>();
       return;
     }
+    const int t = meta[s].t;
+    if (t < 0) break;  // the producer has no more tokens
     const int n = meta[s].n;
-    const int t = (int)item;
     const uint8_t *in = in0 + s * in_stage;
     if constexpr (FP8) {
       uint8_t *out = out0 + s * out_stage;
@@ -351,8 +339,38 @@ __global__ void __launch_bounds__(kMaxConsumers + 32, 1) dispatch_kernel(Dispatc
       if (lane == 0) mbar_arrive(&empty[s]);
     }
   }
-  if (!signalled) tokens_done();
-  if (ctid == 0) bulk_wait_all<0>();
+  // The CTA's tokens are done: publish that their per-token scales are
+  // written and let the scale gather launch.  Then the padding items.
+  if constexpr (FP8 && COL_MAJOR) {
+    if (p.sf_wait == kSfWaitHandshake) {
+      __threadfence();
+      named_barrier(kBarConsumers, nct);
+      if (ctid == 0) atomicAdd(p.sf_sync, 1);
+    }
+  }
+  griddep_launch_dependents();
+  // Padding items, also handed out dynamically; the next index is fetched
+  // while the current item is written.
+  __shared__ int pad_item_s[2];
+  int next_item = 0;
+  if (ctid == 0 && pad_items > 0) next_item = atomicAdd(p.sched + 2, 1);
+  for (int pi = 0; pad_items > 0; ++pi) {
+    if (ctid == 0) pad_item_s[pi & 1] = next_item;
+    named_barrier(kBarConsumers, nct);
+    const int item = pad_item_s[pi & 1];
+    if (item >= pad_items) break;
+    if (ctid == 0) next_item = atomicAdd(p.sched + 2, 1);
+    zero_padding_item(p, item, npad, prow_s[pi & 1], FP8_OUT, COL_MAJOR, ctid, nct);
+  }
+  if (ctid == 0) {
+    bulk_wait_all<0>();
+    // the last CTA resets the scheduler for the next dispatch on the handle
+    if (atomicAdd(p.sched + 1, 1) == (int)gridDim.x - 1) {
+      p.sched[0] = 0;
+      p.sched[1] = 0;
+      p.sched[2] = 0;
+    }
+  }
 }
 
 // Column-major scale factors of every destination row, gathered from the

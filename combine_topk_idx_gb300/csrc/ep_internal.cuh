@@ -14,6 +14,9 @@ constexpr int kLayoutChunkTokens = 256;  // tokens per layout chunk (<= 8192 slo
 
 // Control words at the head of the handle's device block.
 enum CtrlSlot { kCtrlError = 0, kCtrlNumRecv = 2, kCtrlNumExpanded = 3, kCtrlWords = 8 };
+// Handle words shared by dispatch launches: [0, 2) scale-gather handshake,
+// [2, 5) dynamic scheduling (tokens handed out, CTAs finished, padding items).
+constexpr int kDispSyncWords = 5;
 
 // Pinned, device-mapped host words the count wait polls (do_cpu_sync).
 // Mapped host words of the count wait.  Each word is (seq << 32 | value):
@@ -34,8 +37,9 @@ struct LayoutParams {
   int T, K, E, R, L, M, A;
   int do_expand;
   int fixed_cap;          // > 0: fixed-capacity layout, rows per expert (do_expand only)
-  int32_t *disp_sync;     // [2] handle only (else nullptr): dispatch / scale-gather
-                          // handshake counters, zeroed by the layout
+  int32_t *disp_sync;     // [kDispSyncWords] handle only (else nullptr): dispatch
+                          // scheduling and scale-gather handshake counters, zeroed
+                          // by the layout
   int num_blocks;         // layout grid (one CTA per chunk of tokens)
   int blocks_per_src;     // chunks per source rank
   int chunk_tokens;       // tokens per chunk
@@ -98,6 +102,10 @@ struct DispatchParams {
   int32_t *sf_sync;
   int sf_sync_target;
   int sf_wait;
+  // [3] dynamic scheduling: tokens past the first wave handed out, CTAs
+  // finished, padding items handed out (the last CTA resets all three for
+  // the next dispatch on the handle)
+  int32_t *sched;
 };
 
 struct CombineParams {

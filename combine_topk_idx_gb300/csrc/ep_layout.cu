@@ -306,7 +306,7 @@ __global__ void __launch_bounds__(NT, 1) layout_assign_kernel(LayoutParams p) {
       if (r < R) p.cnt_r[r] = tot_s[E + r];
       p.psum_r[r] = scan_s[2 * E + r] - r0;
     }
-    if (p.disp_sync != nullptr && threadIdx.x < 2) p.disp_sync[threadIdx.x] = 0;
+    if (p.disp_sync != nullptr && threadIdx.x < kDispSyncWords) p.disp_sync[threadIdx.x] = 0;
     if (warp == 0) {
       err = __reduce_or_sync(0xffffffffu, err);
       bool over = false;

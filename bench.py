@@ -37,6 +37,7 @@ import ep_workloads as W  # noqa: E402
 
 METRIC = "dispatch & combine HBM GB/s (% of GB300 peak) and tokens/s, 1 GPU"
 L2_FLUSH_BYTES = 256 << 20
+REFERENCE_BUDGET_S = 120.0   # CPU time of a whole `--impl reference` run
 
 
 # ---------------------------------------------------------------------------
@@ -265,14 +266,12 @@ def oracle_step(wl: W.Workload, inp: dict, y_bits):
     return lay
 
 
-def time_oracle(wl: W.Workload, sample_tokens: int, budget_s: float, seed: int = 0):
-    """Run the oracle, as it stands, on the first ``sample_tokens`` tokens of
-    the workload until ``budget_s`` seconds pass (at least once)."""
+def oracle_setup(wl: W.Workload, sample_tokens: int, seed: int = 0):
+    """Inputs of a CPU sample: the first ``sample_tokens`` tokens, and expert
+    outputs for just the rows their routing references."""
     import numpy as np
-    from oracle import ep_oracle as O
     T = min(sample_tokens, wl.num_tokens)
     inp = W.make_inputs(wl, seed=seed, num_tokens=T)
-    # expert outputs: only the rows the routing references are materialised
     lay0 = oracle_layout(wl, inp["topk_idx"].numpy(), sample_tokens_per_rank(wl, T))
     dst = lay0["dst_buffer_slot_idx"]
     need = np.unique(dst[dst >= 0])
@@ -280,6 +279,20 @@ def time_oracle(wl: W.Workload, sample_tokens: int, budget_s: float, seed: int =
     if need.size:
         y_bits[need] = W.hashed_bf16_rows(torch.from_numpy(need), wl.hidden, 7).view(
             torch.int16).numpy().view(np.uint16)
+    return T, inp, y_bits
+
+
+def oracle_sample_text(wl: W.Workload, T: int, seed: int, n: int) -> str:
+    return (f"first {T} tokens of the {wl.name} workload (seed {seed}), full step "
+            f"(layout + dispatch + combine) on 1 core, {n} pass(es)"
+            + (f"; expert capacity {sample_tokens_per_rank(wl, T) * wl.num_ranks} "
+               f"rows (the smallest that holds the sample)" if wl.fixed_capacity else ""))
+
+
+def time_oracle(wl: W.Workload, sample_tokens: int, budget_s: float, seed: int = 0):
+    """Run the oracle, as it stands, on the first ``sample_tokens`` tokens of
+    the workload until ``budget_s`` seconds pass (at least once)."""
+    T, inp, y_bits = oracle_setup(wl, sample_tokens, seed)
     n, t0 = 0, time.perf_counter()
     lay = None
     while True:
@@ -291,10 +304,7 @@ def time_oracle(wl: W.Workload, sample_tokens: int, budget_s: float, seed: int =
     by = bytes_from_layout(wl, T, inp["topk_idx"], lay)
     total = sum(by.values())
     return {"gbs": total / el / 1e9, "tokens_per_s": T / el, "sec_per_step": el, "steps": n,
-            "sample": f"first {T} tokens of the {wl.name} workload (seed {seed}), full step "
-                      f"(layout + dispatch + combine) on 1 core, {n} pass(es)"
-                      + (f"; expert capacity {sample_tokens_per_rank(wl, T) * wl.num_ranks} "
-                         f"rows (the smallest that holds the sample)" if wl.fixed_capacity else "")}
+            "sample": oracle_sample_text(wl, T, seed, n)}
 
 
 def bytes_from_layout(wl, T, topk_idx, lay: dict) -> dict:
@@ -630,15 +640,26 @@ def run_reference(args, ws, rank):
     if rank != 0:
         return
     wl = W.WORKLOADS[args.workload]
+    torch.set_num_threads(1)   # the oracle is timed on one core; so is its setup
+    # One calibration pass (it counts as a warm-up step) sizes the per-step
+    # sample so the whole run stays near REFERENCE_BUDGET_S of CPU time.
+    T = min(args.cpu_sample_tokens, wl.num_tokens)
+    cal = time_oracle(wl, T, 0.0, seed=args.seed)
+    per_step_s = REFERENCE_BUDGET_S / max(1, args.steps + args.warmup)
+    if cal["sec_per_step"] > per_step_s:
+        T = max(32, int(T * per_step_s / cal["sec_per_step"]) // 32 * 32)
+    T, inp, y_bits = oracle_setup(wl, T, args.seed)
     per = []
-    res = None
-    for _ in range(args.warmup):
-        time_oracle(wl, args.cpu_sample_tokens, 0.0, seed=args.seed)
-    for _ in range(args.steps):
-        res = time_oracle(wl, args.cpu_sample_tokens, 0.0, seed=args.seed)
-        per.append(res["sec_per_step"])
+    lay = None
+    for i in range(max(0, args.warmup - 1) + args.steps):
+        t0 = time.perf_counter()
+        lay = oracle_step(wl, inp, y_bits)
+        if i >= max(0, args.warmup - 1):
+            per.append(time.perf_counter() - t0)
     sec = statistics.mean(per)
-    T = args.cpu_sample_tokens
+    total = sum(bytes_from_layout(wl, T, inp["topk_idx"], lay).values())
+    res = {"gbs": total / sec / 1e9, "sec_per_step": sec,
+           "sample": oracle_sample_text(wl, T, args.seed, len(per))}
     gbs = res["gbs"] * res["sec_per_step"] / sec
     line = {
         "impl": "reference", "metric": METRIC, "value": round(gbs, 4), "unit": "GB/s",

@@ -230,21 +230,19 @@ __global__ void __launch_bounds__(NT, 1) layout_assign_kernel(LayoutParams p) {
       if (key < nk) {
         const int32_t *col = key < E ? p.blk_e + key : p.blk_r + (key - E);
         const int stride = key < E ? E : R;
-        int bb = sub;
-        for (; bb + 7 * g < p.num_blocks; bb += 8 * g) {
+        // batches of eight predicated loads, all in flight together
+        for (int bb = sub; bb < p.num_blocks; bb += 8 * g) {
           int v[8];
 #pragma unroll
-          for (int u = 0; u < 8; ++u) v[u] = __ldcg(col + (int64_t)(bb + u * g) * stride);
+          for (int u = 0; u < 8; ++u) {
+            const int c = bb + u * g;
+            v[u] = c < p.num_blocks ? __ldcg(col + (int64_t)c * stride) : 0;
+          }
 #pragma unroll
           for (int u = 0; u < 8; ++u) {
             tot += v[u];
             bef += (bb + u * g < b) ? v[u] : 0;
           }
-        }
-        for (; bb < p.num_blocks; bb += g) {
-          const int v = __ldcg(col + (int64_t)bb * stride);
-          tot += v;
-          bef += (bb < b) ? v : 0;
         }
       }
       for (int o = g >> 1; o > 0; o >>= 1) {

@@ -196,8 +196,9 @@ EP_API ep_status ep_layout(const ep_config *cfg, const void *topk_idx, ep_stream
  *   payload and zero scales.  Rows past the real total are not written.
  * Must be ordered after ep_layout of the same handle (same stream, or the
  *   caller's own event).  May be called again with new x (cached dispatch);
- *   dispatches on one handle must not overlap on the GPU (they share the
- *   handle's scale-gather handshake words).
+ *   dispatches on one handle (this call, ep_dispatch_fp8, ep_combine_backward)
+ *   must not overlap on the GPU: they share the handle's scheduling and
+ *   scale-gather counters.
  */
 EP_API ep_status ep_dispatch(ep_handle *h, const void *x, const float *topk_weights,
                       void *recv_x, float *recv_sf, float *recv_topk_weights,
@@ -215,7 +216,8 @@ EP_API ep_status ep_dispatch(ep_handle *h, const void *x, const float *topk_weig
  * (1, align(T, 4)).  Every destination row gets its token's bytes unchanged
  * and its token's scales in the handle's layout (row-major, or column-major
  * with use_tma_aligned_col_major_sf); padding rows, weights and local expert
- * ids exactly as ep_dispatch.  The other arguments are those of ep_dispatch.
+ * ids exactly as ep_dispatch.  The other arguments are those of ep_dispatch,
+ * and like it, it must not overlap another dispatch of the same handle.
  */
 EP_API ep_status ep_dispatch_fp8(ep_handle *h, const void *x_fp8, const float *x_sf,
                                  int64_t x_sf_token_stride, int64_t x_sf_hidden_stride,
@@ -277,7 +279,8 @@ EP_API ep_status ep_dispatch_backward(const ep_handle *h, const void *grad_recv_
  *   destination row gets its token's gradient row, bit for bit.  Always a
  *   BF16 copy, also when cfg->use_fp8 quantises the forward dispatch.
  *   Padding rows (expanded) are zeroed when cfg->do_zero_padding, else left
- *   as they are; rows past the real total are not written.
+ *   as they are; rows past the real total are not written.  Like ep_dispatch,
+ *   it must not overlap another dispatch of the same handle.
  */
 EP_API ep_status ep_combine_backward(ep_handle *h, const void *grad_combined_x,
                                      void *grad_recv_x, ep_stream_t stream);

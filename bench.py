@@ -307,6 +307,45 @@ def time_oracle(wl: W.Workload, sample_tokens: int, budget_s: float, seed: int =
             "sample": oracle_sample_text(wl, T, seed, n)}
 
 
+def _oracle_worker(job):
+    """One process of the all-cores oracle timing (spawned, one thread)."""
+    name, tokens, budget, seed = job
+    torch.set_num_threads(1)
+    r = time_oracle(W.WORKLOADS[name], tokens, budget, seed=seed)
+    return r["gbs"], r["tokens_per_s"]
+
+
+def time_oracle_all_cores(wl: W.Workload, sample_tokens: int, budget_s: float, seed: int):
+    """The oracle on every host core at once: one spawned process per core,
+    each timing its own sample (seeds seed, seed + 1, ...); the aggregate
+    throughput is the sum.  None if no process pool can be started."""
+    import multiprocessing as mp
+    n = os.cpu_count() or 1
+    try:
+        with mp.get_context("spawn").Pool(n) as pool:
+            res = pool.map(_oracle_worker, [(wl.name, sample_tokens, budget_s, seed + i)
+                                             for i in range(n)])
+    except Exception:
+        return None
+    return {"value": round(sum(g for g, _ in res), 4), "unit": "GB/s", "cores": n,
+            "kind": "oracle", "tokens_per_s": round(sum(t for _, t in res), 1),
+            "cpu_model": cpu_model(),
+            "sample": f"{n} processes, each the first {min(sample_tokens, wl.num_tokens)} tokens "
+                      f"of the {wl.name} workload with its own seed, for {budget_s:g} s"}
+
+
+def cpu_model() -> str:
+    try:
+        out = subprocess.run(["lscpu"], capture_output=True, text=True, timeout=10).stdout
+        for ln in out.splitlines():
+            if ln.startswith("Model name:"):
+                return ln.split(":", 1)[1].strip()
+    except (OSError, subprocess.SubprocessError):
+        pass
+    import platform
+    return platform.processor() or platform.machine()
+
+
 def bytes_from_layout(wl, T, topk_idx, lay: dict) -> dict:
     import numpy as np
     dst = lay["dst_buffer_slot_idx"]
@@ -382,21 +421,28 @@ def run_gpu(args, ws, rank, local):
     h0.free()
     del out0
 
-    def one_step(timed: bool, ev=None):
-        flush_l2()
+    layout_host_s = []
+
+    def one_step(timed: bool, ev=None, flush=True):
+        if flush:
+            flush_l2()
         if timed:
             ev[0].record(stream)
+        t_host = time.perf_counter()
         h = ep.ep_layout(cfg, idx)
         if timed:
+            layout_host_s.append(time.perf_counter() - t_host)
             ev[1].record(stream)
         out = ep.alloc_recv(h, with_weights=True, with_idx=True)
-        flush_l2()
+        if flush:
+            flush_l2()
         if timed:
             ev[2].record(stream)
         ep.ep_dispatch(h, x, w, **out)
         if timed:
             ev[3].record(stream)
-        flush_l2()
+        if flush:
+            flush_l2()
         if timed:
             ev[4].record(stream)
         ep.ep_combine(h, y, w, None, None, eb, out=out_comb)
@@ -431,6 +477,18 @@ def run_gpu(args, ws, rank, local):
     step_ms_max = max_over_ranks(step_ms, ws, dev)
     total_bytes = sum(by.values())
     value = total_bytes * ws / (step_ms_max * 1e-3) / 1e9
+
+    # Secondary: warm L2 (no flush between stages), same step, untimed warm-up.
+    warm_steps = max(8, args.steps // 8)
+    for _ in range(3):
+        one_step(False, flush=False)
+    wev = [[torch.cuda.Event(enable_timing=True) for _ in range(6)] for _ in range(warm_steps)]
+    torch.cuda.synchronize()
+    for i in range(warm_steps):
+        one_step(True, wev[i], flush=False)
+    torch.cuda.synchronize()
+    warm = {k: statistics.mean(e[a].elapsed_time(e[b]) for e in wev)
+            for k, a, b in (("layout", 0, 1), ("dispatch", 2, 3), ("combine", 4, 5))}
 
     # e2e through the C ABI with host buffers: every step copies its inputs
     # (topk_idx, topk_weights, x) in from pinned host memory and its combined
@@ -594,6 +652,11 @@ def run_gpu(args, ws, rank, local):
                         "gbs": round(by["combine"] / c_ms / 1e6, 1),
                         "frac_of_peak": round(by["combine"] / c_ms / 1e6 / peaks["hbm_gbs"], 4)},
         },
+        "layout_plus_dispatch_ms": round(statistics.mean(lay_ms) + d_ms, 5),
+        "layout_host_ms": round(1e3 * statistics.median(layout_host_s), 5),
+        "warm_l2": {"steps": warm_steps,
+                    **{k: {"ms": round(v, 5), "gbs": round(by[k] / v / 1e6, 1)}
+                       for k, v in warm.items()}},
         "roofline": {"bound": "hbm", "kernel": dom, "achieved": round(achieved, 1),
                      "peak": peaks["hbm_gbs"], "peak_source": peaks["source"], "unit": "GB/s",
                      "frac": round(achieved / peaks["hbm_gbs"], 4), "traffic": traffic,
@@ -628,7 +691,11 @@ def run_gpu(args, ws, rank, local):
         cb = time_oracle(wl, args.cpu_sample_tokens, args.cpu_budget_s, seed=args.seed)
         line["cpu_baseline"] = {"value": round(cb["gbs"], 4), "unit": "GB/s", "cores": 1,
                                 "kind": "oracle", "sample": cb["sample"],
-                                "tokens_per_s": round(cb["tokens_per_s"], 1)}
+                                "tokens_per_s": round(cb["tokens_per_s"], 1),
+                                "cpu_model": cpu_model()}
+        allc = time_oracle_all_cores(wl, args.cpu_sample_tokens, args.cpu_budget_s, args.seed)
+        if allc is not None:
+            line["cpu_baseline_all_cores"] = allc
     if ws > 1:
         torch.distributed.destroy_process_group()
     if rank == 0:

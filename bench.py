@@ -421,17 +421,13 @@ def run_gpu(args, ws, rank, local):
     h0.free()
     del out0
 
-    layout_host_s = []
-
     def one_step(timed: bool, ev=None, flush=True):
         if flush:
             flush_l2()
         if timed:
             ev[0].record(stream)
-        t_host = time.perf_counter()
         h = ep.ep_layout(cfg, idx)
         if timed:
-            layout_host_s.append(time.perf_counter() - t_host)
             ev[1].record(stream)
         out = ep.alloc_recv(h, with_weights=True, with_idx=True)
         if flush:
@@ -489,6 +485,16 @@ def run_gpu(args, ws, rank, local):
     torch.cuda.synchronize()
     warm = {k: statistics.mean(e[a].elapsed_time(e[b]) for e in wev)
             for k, a, b in (("layout", 0, 1), ("dispatch", 2, 3), ("combine", 4, 5))}
+    # Host wall time of the layout call on an idle GPU (with do_cpu_sync it
+    # includes the count wait).
+    layout_host_s = []
+    for _ in range(20):
+        torch.cuda.synchronize()
+        t_host = time.perf_counter()
+        h = ep.ep_layout(cfg, idx)
+        layout_host_s.append(time.perf_counter() - t_host)
+        h.free()
+    torch.cuda.synchronize()
 
     # e2e through the C ABI with host buffers: every step copies its inputs
     # (topk_idx, topk_weights, x) in from pinned host memory and its combined

@@ -6,8 +6,9 @@
 // payload is e4m3 with one fp32 scale per 1x128 block (scale = amax / 448).
 //
 // Token-major scatter with persistent, warp-specialised CTAs:
-//   warp 0 (producer) takes the CTA's tokens in turn, reads each token's K
-//     destination rows (prefetched four tokens ahead), keeps the distinct ones
+//   warp 0 (producer) takes tokens -- the CTA's index first, then the next
+//     free one from a handle counter -- reads each token's K destination rows
+//     (the next token's while the current one is issued), keeps the distinct ones
 //     (rank-layout slots of one rank share a row), writes the per-row weights
 //     and local expert ids, and issues one cp.async.bulk global->shared copy
 //     of the token's source row into a ring of kStages input stages;
@@ -24,7 +25,8 @@
 //           column-major gather, which then reads the caller's scales.
 // The source row is read from HBM once and quantised once whatever K is; the
 // TMA engine moves every payload byte.  After the tokens, the consumer warps
-// zero the alignment padding rows in 8-row work items.  Every mbarrier wait
+// zero the alignment padding rows in 8-row work items, also handed out from a
+// handle counter.  Every mbarrier wait
 // is bounded: a wait that gives up sets EP_ERRBIT_TIMEOUT and the CTA returns.
 #include <algorithm>
 

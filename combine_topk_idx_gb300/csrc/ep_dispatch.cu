@@ -11,7 +11,8 @@
 //     (the next token's while the current one is issued), keeps the distinct ones
 //     (rank-layout slots of one rank share a row), writes the per-row weights
 //     and local expert ids, and issues one cp.async.bulk global->shared copy
-//     of the token's source row into a ring of kStages input stages;
+//     of the token's source row into a ring of input stages (3; 2 for
+//     quantised rows too large for three);
 //   the consumer warps wait for a stage and
 //     FP8:  quantise it -- amax of each 128-element block by a 16-lane
 //           shuffle, scale = amax / 448 and x / scale with IEEE divisions,
@@ -36,7 +37,8 @@
 namespace ep {
 namespace {
 
-constexpr int kStages = 3;
+constexpr int kMaxStages = 3;          // stage ring depth, or 2 when 3 do not fit
+constexpr size_t kSmemLimit = 227 * 1024 - 4096;  // dynamic share, static arrays set aside
 constexpr int kPadRowsPerItem = 8;
 constexpr int kMaxConsumers = 224;
 constexpr int kWaitIters = 4000;          // x kWaitHintNs: gives up after ~2 s
@@ -130,9 +132,9 @@ __global__ void __launch_bounds__(kMaxConsumers + 32, 1) dispatch_kernel(Dispatc
   constexpr bool FP8 = MODE == kModeQuant;         // quantise in the consumers
   constexpr bool FP8_OUT = MODE != kModeBf16;      // e4m3 payload + scales
   extern __shared__ __align__(128) uint8_t smem[];
-  __shared__ __align__(8) uint64_t full[kStages];
-  __shared__ __align__(8) uint64_t empty[kStages];
-  __shared__ TokenMeta meta[kStages];
+  __shared__ __align__(8) uint64_t full[kMaxStages];
+  __shared__ __align__(8) uint64_t empty[kMaxStages];
+  __shared__ TokenMeta meta[kMaxStages];
   __shared__ int prow_s[2][kPadRowsPerItem];
 
   const int H = p.H;
@@ -142,14 +144,15 @@ __global__ void __launch_bounds__(kMaxConsumers + 32, 1) dispatch_kernel(Dispatc
   const int out_stage = FP8 ? (H + 127) / 128 * 128 : 0;
   const int nb = H / kFp8Block;
   const int nb_pad = (nb + 31) / 32 * 32;
+  const int S = p.stages;
   uint8_t *in0 = smem;
-  uint8_t *out0 = smem + kStages * in_stage;
-  float *sf0 = reinterpret_cast<float *>(out0 + kStages * out_stage);  // row-major scales
+  uint8_t *out0 = smem + S * in_stage;
+  float *sf0 = reinterpret_cast<float *>(out0 + S * out_stage);  // row-major scales
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
   const int ncw = (blockDim.x >> 5) - 1;
 
   if (threadIdx.x == 0) {
-    for (int s = 0; s < kStages; ++s) {
+    for (int s = 0; s < S; ++s) {
       mbar_init(&full[s], 1);
       mbar_init(&empty[s], ncw);
     }
@@ -173,8 +176,8 @@ __global__ void __launch_bounds__(kMaxConsumers + 32, 1) dispatch_kernel(Dispatc
     for (int64_t i = 0;; ++i) {
       const int t = next;
       const Routing cur = rn;
-      const int s = (int)(i % kStages);
-      const int64_t k = i / kStages;
+      const int s = (int)(i % S);
+      const int64_t k = i / S;
       if (k > 0) {
         bool ok = false;
         if (lane == 0)
@@ -244,8 +247,8 @@ __global__ void __launch_bounds__(kMaxConsumers + 32, 1) dispatch_kernel(Dispatc
   const int64_t pad_items = (npad + kPadRowsPerItem - 1) / kPadRowsPerItem;
   uint8_t *recv = static_cast<uint8_t *>(p.recv_x);
   for (int64_t i = 0;; ++i) {
-    const int s = (int)(i % kStages);
-    const uint32_t par = (uint32_t)((i / kStages) & 1);
+    const int s = (int)(i % S);
+    const uint32_t par = (uint32_t)((i / S) & 1);
     if (!mbar_wait_bounded(&full[s], par, kWaitIters, kWaitHintNs)) {
       if (lane == 0) atomicOr(p.err, EP_ERRBIT_TIMEOUT);
       if (ctid == 0) bulk_wait_all<0>();
@@ -259,7 +262,10 @@ __global__ void __launch_bounds__(kMaxConsumers + 32, 1) dispatch_kernel(Dispatc
       uint8_t *out = out0 + s * out_stage;
       float *sf = sf0 + s * nb_pad;
       if (n > 0) {
-        if (ctid == 0) bulk_wait_read<kStages - 1>();  // out stage s no longer read
+        // out stage s no longer read: at most S - 1 later bulk groups pending
+        if (ctid == 0) {
+          if (S == kMaxStages) bulk_wait_read<kMaxStages - 1>(); else bulk_wait_read<1>();
+        }
         named_barrier(kBarConsumers, nct);
         // every consumer thread runs the same number of iterations so the
         // 16-lane shuffles always see full warps (nvec and nct are multiples of 16)
@@ -497,8 +503,10 @@ cudaError_t launch_one(const DispatchParams &p0, int sm_cap, cudaStream_t s) {
   const int threads = consumers + 32;
   const size_t in_stage = (size_t)((MODE == kModePreq ? H : 2 * H) + 127) / 128 * 128;
   const size_t out_stage = FP8 ? (size_t)(H + 127) / 128 * 128 : 0;
-  const size_t smem = kStages * (in_stage + out_stage) +
-                      (FP8 && !CM ? kStages * sizeof(float) * ((H / kFp8Block + 31) / 32 * 32) : 0);
+  const size_t sf_stage = FP8 && !CM ? sizeof(float) * ((H / kFp8Block + 31) / 32 * 32) : 0;
+  // quantising rows of the largest hidden sizes (above ~24K) take two stages
+  p.stages = kMaxStages * (in_stage + out_stage + sf_stage) <= kSmemLimit ? kMaxStages : 2;
+  const size_t smem = p.stages * (in_stage + out_stage + sf_stage);
   cudaError_t err;
   if (smem > kDynSmemOptIn) {
     err = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);

@@ -412,3 +412,33 @@ def test_shared_memory_window_edges(ep):
     idx, w = _routing(T, K, E, seed=22)
     x = torch.randn(T, H, generator=torch.Generator().manual_seed(3)).to(torch.bfloat16)
     run_and_check(ep, ep.make_config(T, K, E, R, H, M, 1, False, False, True), idx, x, w)
+
+
+@pytest.mark.parametrize("fp8,cm", [(True, True), (True, False), (False, False)])
+def test_maximum_hidden(ep, fp8, cm):
+    """The largest hidden size the configuration accepts (32768): a quantising
+    dispatch needs more shared memory per stage than three stages leave room
+    for, so its stage ring is shorter; every output still matches the oracle
+    (with a per-expert bias in the combine)."""
+    T, K, E, R, H, M = 40, 4, 8, 2, 32768, 20
+    idx, w = _routing(T, K, E, seed=23, drop=0.1)
+    x = torch.randn(T, H, generator=torch.Generator().manual_seed(4)).to(torch.bfloat16)
+    eb = W.hashed_bf16_rows(torch.arange(E), H, 19)
+    run_and_check(ep, ep.make_config(T, K, E, R, H, M, 8, True, True, True, fp8, cm),
+                  idx, x, w, expert_bias=eb)
+
+
+@pytest.mark.parametrize("cm_in", [False, True])
+def test_maximum_hidden_prequantised(ep, cm_in):
+    from tests.test_prequant_gpu import run_prequant
+    T, K, E, R, H, M = 40, 4, 8, 2, 32768, 20
+    idx, w = _routing(T, K, E, seed=24, drop=0.1)
+    run_prequant(ep, ep.make_config(T, K, E, R, H, M, 8, True, True, False, True, True),
+                 idx, w, cm_in)
+
+
+def test_maximum_hidden_backward_pair(ep):
+    from tests.test_backward_gpu import check_backward
+    T, K, E, R, H, M = 40, 4, 8, 2, 32768, 20
+    idx, _ = _routing(T, K, E, seed=25, drop=0.1)
+    check_backward(ep, ep.make_config(T, K, E, R, H, M, 8, True, True, False, False, False), idx)

@@ -16,10 +16,11 @@
 //   the other warps (consumers) wait for a stage and accumulate its rows
 //     strictly in slot order -- per-expert bias added to each row first (a
 //     small table reused by every token: read through L1, not staged), then
-//     separately rounded fp32 multiplies and adds (__fmul_rn / __fadd_rn: no
-//     FMA contraction) -- add the per-token biases, round to BF16 (nearest
-//     even), store the output chunk and release the stage on its "empty"
-//     mbarrier.
+//     separately rounded fp32 multiplies and adds (__fmul_rn / __fadd_rn:
+//     never contracted to an FMA; the compiler may fuse a packed f32x2
+//     multiply into a following packed add, so packed adds serve only the
+//     bias sum) -- add the per-token biases, round to BF16 (nearest even),
+//     store the output chunk and release the stage on its "empty" mbarrier.
 // Each output element is written by exactly one thread: no atomics.  Every
 // mbarrier wait is bounded; a wait that gives up sets EP_ERRBIT_TIMEOUT in
 // the handle's error word and the CTA returns.
@@ -51,16 +52,27 @@ __device__ __forceinline__ void unpack8(const uint4 &v, float *f) {
   f[6] = bf16_lo(v.w); f[7] = bf16_hi(v.w);
 }
 
+// Eight BF16 pairs summed in fp32, element by element (each sum rounded to
+// nearest even), with packed f32x2 adds.
+__device__ __forceinline__ void add8_bf16(const uint4 &a, const uint4 &b, float *f) {
+  const uint64_t s0 = f32x2_add_rn(bf16x2_to_f32x2(a.x), bf16x2_to_f32x2(b.x));
+  const uint64_t s1 = f32x2_add_rn(bf16x2_to_f32x2(a.y), bf16x2_to_f32x2(b.y));
+  const uint64_t s2 = f32x2_add_rn(bf16x2_to_f32x2(a.z), bf16x2_to_f32x2(b.z));
+  const uint64_t s3 = f32x2_add_rn(bf16x2_to_f32x2(a.w), bf16x2_to_f32x2(b.w));
+  f[0] = f32x2_lo(s0); f[1] = f32x2_hi(s0);
+  f[2] = f32x2_lo(s1); f[3] = f32x2_hi(s1);
+  f[4] = f32x2_lo(s2); f[5] = f32x2_hi(s2);
+  f[6] = f32x2_lo(s3); f[7] = f32x2_hi(s3);
+}
+
 struct Routing {
   int d, e;
   float w;
 };
 
 template <bool HAS_W, bool HAS_EB>
-__device__ __forceinline__ Routing load_routing(const CombineParams &p, int64_t unit, int nchunks,
-                                                int lane) {
+__device__ __forceinline__ Routing load_routing(const CombineParams &p, int64_t t, int lane) {
   Routing r{-1, -1, 1.f};
-  const int64_t t = unit / nchunks;
   if (lane < p.K) {
     r.d = __ldg(p.dst + t * p.K + lane);
     if (HAS_EB) r.e = __ldg(p.topk32 + t * p.K + lane);
@@ -68,6 +80,31 @@ __device__ __forceinline__ Routing load_routing(const CombineParams &p, int64_t 
   }
   return r;
 }
+
+// A CTA's current unit u and its (token t, chunk c), advanced by the grid
+// stride G.  STEP: with adds only (gq whole tokens and gr chunks per stride);
+// otherwise t and c are recomputed from u by a 64-bit division.
+template <bool STEP>
+struct UnitCursor {
+  int64_t u;
+  int t, c;
+  __device__ __forceinline__ UnitCursor(int64_t u0, int nchunks)
+      : u(u0), t((int)(u0 / nchunks)), c((int)(u0 % nchunks)) {}
+  __device__ __forceinline__ void advance(int64_t G, int gq, int gr, int nchunks) {
+    u += G;
+    if (STEP) {
+      t += gq;
+      c += gr;
+      if (c >= nchunks) {
+        c -= nchunks;
+        ++t;
+      }
+    } else {
+      t = (int)(u / nchunks);
+      c = (int)(u - (int64_t)t * nchunks);
+    }
+  }
+};
 
 template <bool HAS_W, bool HAS_EB>
 __global__ void __launch_bounds__(kMaxConsumers + 32, 1)
@@ -80,7 +117,12 @@ __global__ void __launch_bounds__(kMaxConsumers + 32, 1)
   const int H = p.H;
   const int64_t row_bytes = 2 * (int64_t)H;
   const int64_t stage_bytes = (int64_t)slots_cap * chunk_bytes;
-  const int64_t num_units = (int64_t)p.T * nchunks;
+  // The expert-bias combine is bound by instruction issue, so it steps its
+  // units without divisions.  The others keep the division: stepping there
+  // measured 2-3 us slower on the HBM-bound 4096 x 7168 top-8 combine.
+  using Cursor = UnitCursor<HAS_EB>;
+  const int64_t G = gridDim.x;
+  const int gq = (int)(G / nchunks), gr = (int)(G % nchunks);
   const int has_b0 = p.bias0 != nullptr, has_b1 = p.bias1 != nullptr;
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
   const int ncw = (blockDim.x >> 5) - 1;  // consumer warps
@@ -98,19 +140,23 @@ __global__ void __launch_bounds__(kMaxConsumers + 32, 1)
     // ---------------- producer ----------------
     const uint64_t stream_pol = l2_policy_evict_first();  // expert outputs are read once
     // routing of the next four units is in flight while one is issued
-    int64_t u = blockIdx.x;
-    const int64_t G = gridDim.x;
+    // (ahead: the unit whose routing was loaded last)
+    Cursor u(blockIdx.x, nchunks), ahead(blockIdx.x, nchunks);
     Routing r0{-1, -1, 1.f}, r1{-1, -1, 1.f}, r2{-1, -1, 1.f}, r3{-1, -1, 1.f};
-    if (u < num_units) r0 = load_routing<HAS_W, HAS_EB>(p, u, nchunks, lane);
-    if (u + G < num_units) r1 = load_routing<HAS_W, HAS_EB>(p, u + G, nchunks, lane);
-    if (u + 2 * G < num_units) r2 = load_routing<HAS_W, HAS_EB>(p, u + 2 * G, nchunks, lane);
-    if (u + 3 * G < num_units) r3 = load_routing<HAS_W, HAS_EB>(p, u + 3 * G, nchunks, lane);
-    for (int64_t i = 0; u < num_units; ++i, u += G) {
+    if (ahead.t < p.T) r0 = load_routing<HAS_W, HAS_EB>(p, ahead.t, lane);
+    ahead.advance(G, gq, gr, nchunks);
+    if (ahead.t < p.T) r1 = load_routing<HAS_W, HAS_EB>(p, ahead.t, lane);
+    ahead.advance(G, gq, gr, nchunks);
+    if (ahead.t < p.T) r2 = load_routing<HAS_W, HAS_EB>(p, ahead.t, lane);
+    ahead.advance(G, gq, gr, nchunks);
+    if (ahead.t < p.T) r3 = load_routing<HAS_W, HAS_EB>(p, ahead.t, lane);
+    for (int64_t i = 0; u.t < p.T; ++i, u.advance(G, gq, gr, nchunks)) {
       const Routing cur = r0;
       r0 = r1;
       r1 = r2;
       r2 = r3;
-      if (u + 4 * G < num_units) r3 = load_routing<HAS_W, HAS_EB>(p, u + 4 * G, nchunks, lane);
+      ahead.advance(G, gq, gr, nchunks);
+      if (ahead.t < p.T) r3 = load_routing<HAS_W, HAS_EB>(p, ahead.t, lane);
       const int s = (int)(i % kStages);
       const int64_t k = i / kStages;
       if (k > 0) {
@@ -123,8 +169,8 @@ __global__ void __launch_bounds__(kMaxConsumers + 32, 1)
           return;
         }
       }
-      const int64_t t = u / nchunks;
-      const int64_t off = (u - t * nchunks) * (int64_t)chunk_bytes;
+      const int64_t t = u.t;
+      const int64_t off = (int64_t)u.c * chunk_bytes;
       const uint32_t bytes = (uint32_t)min((int64_t)chunk_bytes, row_bytes - off);
       bool use = cur.d >= 0;
       if (!HAS_W) {  // weights already applied: each row counts once
@@ -171,15 +217,15 @@ __global__ void __launch_bounds__(kMaxConsumers + 32, 1)
   const int ctid = threadIdx.x - 32;
   const int cthreads = blockDim.x - 32;
   int64_t i = 0;
-  for (int64_t u = blockIdx.x; u < num_units; u += gridDim.x, ++i) {
+  for (Cursor u(blockIdx.x, nchunks); u.t < p.T; u.advance(G, gq, gr, nchunks), ++i) {
     const int s = (int)(i % kStages);
     const uint32_t par = (uint32_t)((i / kStages) & 1);
     if (!mbar_wait_bounded(&full[s], par, kWaitIters, kWaitHintNs)) {
       if (lane == 0) atomicOr(p.err, EP_ERRBIT_TIMEOUT);
       return;
     }
-    const int64_t t = u / nchunks;
-    const int64_t off = (u - t * nchunks) * (int64_t)chunk_bytes;
+    const int64_t t = u.t;
+    const int64_t off = (int64_t)u.c * chunk_bytes;
     const int nv = (int)(min((int64_t)chunk_bytes, row_bytes - off) / 16);
     const int n = meta[s].n;
     const uint8_t *sb = smem + s * stage_bytes;
@@ -189,12 +235,13 @@ __global__ void __launch_bounds__(kMaxConsumers + 32, 1)
       for (int q = 0; q < 8; ++q) acc[q] = 0.f;
       for (int j = 0; j < n; ++j) {
         float f[8];
-        unpack8(*reinterpret_cast<const uint4 *>(sb + (int64_t)j * chunk_bytes + v * 16), f);
         if (HAS_EB) {
-          float b[8];
-          unpack8(ld_cached_v4(p.ebias + (int64_t)meta[s].e[j] * H + off / 2 + v * 8), b);
-#pragma unroll
-          for (int q = 0; q < 8; ++q) f[q] = __fadd_rn(f[q], b[q]);
+          // y + expert bias, two lanes per packed add (no multiply feeds it,
+          // so nothing can be contracted)
+          const uint4 bv = ld_cached_v4(p.ebias + (int64_t)meta[s].e[j] * H + off / 2 + v * 8);
+          add8_bf16(*reinterpret_cast<const uint4 *>(sb + (int64_t)j * chunk_bytes + v * 16), bv, f);
+        } else {
+          unpack8(*reinterpret_cast<const uint4 *>(sb + (int64_t)j * chunk_bytes + v * 16), f);
         }
         if (HAS_W) {
           const float w = meta[s].w[j];

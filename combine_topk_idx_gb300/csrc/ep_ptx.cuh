@@ -81,6 +81,40 @@ __device__ __forceinline__ uint32_t cvt_bf16x2(float lo, float hi) {
 __device__ __forceinline__ float bf16_lo(uint32_t w) { return __uint_as_float(w << 16); }
 __device__ __forceinline__ float bf16_hi(uint32_t w) { return __uint_as_float(w & 0xffff0000u); }
 
+// Two fp32 lanes in one 64-bit register (lane 0 in the low word), for the
+// packed f32x2 arithmetic of sm_100 and later: each lane is rounded to
+// nearest even exactly like the scalar add.rn.f32 / mul.rn.f32, and no
+// multiply-add is ever contracted.
+__device__ __forceinline__ uint64_t f32x2_pack(float lo, float hi) {
+  uint64_t r;
+  asm("mov.b64 %0, {%1, %2};" : "=l"(r) : "f"(lo), "f"(hi));
+  return r;
+}
+__device__ __forceinline__ float f32x2_lo(uint64_t v) {
+  float lo, hi;
+  asm("mov.b64 {%0, %1}, %2;" : "=f"(lo), "=f"(hi) : "l"(v));
+  return lo;
+}
+__device__ __forceinline__ float f32x2_hi(uint64_t v) {
+  float lo, hi;
+  asm("mov.b64 {%0, %1}, %2;" : "=f"(lo), "=f"(hi) : "l"(v));
+  return hi;
+}
+__device__ __forceinline__ uint64_t f32x2_add_rn(uint64_t a, uint64_t b) {
+  uint64_t d;
+  asm("add.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
+  return d;
+}
+__device__ __forceinline__ uint64_t f32x2_mul_rn(uint64_t a, uint64_t b) {
+  uint64_t d;
+  asm("mul.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
+  return d;
+}
+// A BF16 pair (element 0 in the low half) -> two fp32 lanes (exact).
+__device__ __forceinline__ uint64_t bf16x2_to_f32x2(uint32_t w) {
+  return f32x2_pack(bf16_lo(w), bf16_hi(w));
+}
+
 __device__ __forceinline__ uint32_t lanemask_lt() {
   uint32_t r;
   asm("mov.u32 %0, %%lanemask_lt;" : "=r"(r));

@@ -37,7 +37,7 @@
 namespace ep {
 namespace {
 
-constexpr int kMaxStages = 3;          // stage ring depth, or 2 when 3 do not fit
+constexpr int kStages = 3;              // stage ring depth (2 where 3 do not fit)
 constexpr size_t kSmemLimit = 227 * 1024 - 4096;  // dynamic share, static arrays set aside
 constexpr int kPadRowsPerItem = 8;
 constexpr int kMaxConsumers = 224;
@@ -127,14 +127,14 @@ __device__ __forceinline__ Routing load_routing(const DispatchParams &p, int t, 
   return r;
 }
 
-template <int MODE, bool COL_MAJOR>
+template <int MODE, bool COL_MAJOR, int S>
 __global__ void __launch_bounds__(kMaxConsumers + 32, 1) dispatch_kernel(DispatchParams p) {
   constexpr bool FP8 = MODE == kModeQuant;         // quantise in the consumers
   constexpr bool FP8_OUT = MODE != kModeBf16;      // e4m3 payload + scales
   extern __shared__ __align__(128) uint8_t smem[];
-  __shared__ __align__(8) uint64_t full[kMaxStages];
-  __shared__ __align__(8) uint64_t empty[kMaxStages];
-  __shared__ TokenMeta meta[kMaxStages];
+  __shared__ __align__(8) uint64_t full[S];
+  __shared__ __align__(8) uint64_t empty[S];
+  __shared__ TokenMeta meta[S];
   __shared__ int prow_s[2][kPadRowsPerItem];
 
   const int H = p.H;
@@ -144,7 +144,6 @@ __global__ void __launch_bounds__(kMaxConsumers + 32, 1) dispatch_kernel(Dispatc
   const int out_stage = FP8 ? (H + 127) / 128 * 128 : 0;
   const int nb = H / kFp8Block;
   const int nb_pad = (nb + 31) / 32 * 32;
-  const int S = p.stages;
   uint8_t *in0 = smem;
   uint8_t *out0 = smem + S * in_stage;
   float *sf0 = reinterpret_cast<float *>(out0 + S * out_stage);  // row-major scales
@@ -263,9 +262,7 @@ __global__ void __launch_bounds__(kMaxConsumers + 32, 1) dispatch_kernel(Dispatc
       float *sf = sf0 + s * nb_pad;
       if (n > 0) {
         // out stage s no longer read: at most S - 1 later bulk groups pending
-        if (ctid == 0) {
-          if (S == kMaxStages) bulk_wait_read<kMaxStages - 1>(); else bulk_wait_read<1>();
-        }
+        if (ctid == 0) bulk_wait_read<S - 1>();
         named_barrier(kBarConsumers, nct);
         // every consumer thread runs the same number of iterations so the
         // 16-lane shuffles always see full warps (nvec and nct are multiples of 16)
@@ -489,7 +486,6 @@ __global__ void __launch_bounds__(256) sf_expand_kernel(DispatchParams p) {
 template <int MODE, bool CM>
 cudaError_t launch_one(const DispatchParams &p0, int sm_cap, cudaStream_t s) {
   constexpr bool FP8 = MODE == kModeQuant;
-  auto kern = dispatch_kernel<MODE, CM>;
   DispatchParams p = p0;
   // the scale gather reads 4 scales of a token at once when they are
   // contiguous and 16-byte aligned
@@ -505,8 +501,15 @@ cudaError_t launch_one(const DispatchParams &p0, int sm_cap, cudaStream_t s) {
   const size_t out_stage = FP8 ? (size_t)(H + 127) / 128 * 128 : 0;
   const size_t sf_stage = FP8 && !CM ? sizeof(float) * ((H / kFp8Block + 31) / 32 * 32) : 0;
   // quantising rows of the largest hidden sizes (above ~24K) take two stages
-  p.stages = kMaxStages * (in_stage + out_stage + sf_stage) <= kSmemLimit ? kMaxStages : 2;
-  const size_t smem = p.stages * (in_stage + out_stage + sf_stage);
+  auto kern = dispatch_kernel<MODE, CM, kStages>;
+  int stages = kStages;
+  if constexpr (FP8) {
+    if (kStages * (in_stage + out_stage + sf_stage) > kSmemLimit) {
+      kern = dispatch_kernel<MODE, CM, 2>;
+      stages = 2;
+    }
+  }
+  const size_t smem = stages * (in_stage + out_stage + sf_stage);
   cudaError_t err;
   if (smem > kDynSmemOptIn) {
     err = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);

@@ -106,9 +106,6 @@ struct DispatchParams {
   // finished, padding items handed out (the last CTA resets all three for
   // the next dispatch on the handle)
   int32_t *sched;
-  // depth of the input/output stage ring (2 or 3: 3 unless that does not fit
-  // in shared memory)
-  int stages;
 };
 
 struct CombineParams {

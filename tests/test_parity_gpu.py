@@ -442,3 +442,21 @@ def test_maximum_hidden_backward_pair(ep):
     T, K, E, R, H, M = 40, 4, 8, 2, 32768, 20
     idx, _ = _routing(T, K, E, seed=25, drop=0.1)
     check_backward(ep, ep.make_config(T, K, E, R, H, M, 8, True, True, False, False, False), idx)
+
+
+@pytest.mark.parametrize("expand", [False, True])
+def test_expert_bias_combine_grid_strides(ep, expand):
+    """The per-expert-bias combine steps each CTA's (token, chunk) by the grid
+    stride with adds only.  Hidden 7168 splits into 7 chunks (10 with a
+    per-token bias); capping the grid at 1 and 3 SMs, and the full grid, gives
+    strides of fewer chunks than a row, strides that wrap a row end, and
+    several units per CTA.  Every output against the oracle."""
+    T, K, E, R, H, M = 600, 8, 32, 4, 7168, 150
+    idx, w = _routing(T, K, E, seed=26, drop=0.05)
+    x = torch.randn(T, H, generator=torch.Generator().manual_seed(6)).to(torch.bfloat16)
+    eb = W.hashed_bf16_rows(torch.arange(E), H, 27)
+    for sms in (1, 3, 0):
+        for b0 in (False, True):
+            cfg = ep.make_config(T, K, E, R, H, M, 4 if expand else 1, expand, expand, True,
+                                 num_sms=sms)
+            run_and_check(ep, cfg, idx, x, w, bias0=b0, expert_bias=eb)

@@ -352,6 +352,13 @@ def quantize_row(x_bits):
     (IEEE division, RNE); q = e4m3(x / scale) with an fp32 IEEE division
     (reading R8: a true division, not a multiply by 448 / amax).  An all-zero
     block has scale 0 and all bytes 0x00 (reading R9).
+
+    Non-finite inputs (reading R16; the pages do not mention them): the amax
+    propagates NaN, so a block holding a NaN has a NaN scale and every
+    quotient is NaN; a block whose amax is infinite has scale +inf, its
+    finite elements divide to +-0 and its infinite ones to NaN.  Every NaN
+    quotient encodes as 0x7F, whatever the sign bit IEEE division left on
+    it (that sign differs between hosts).
     """
     x = bf16_bits_to_f32(x_bits)
     H = x.shape[-1]
@@ -363,6 +370,8 @@ def quantize_row(x_bits):
     zero = scale == 0
     with np.errstate(divide="ignore", invalid="ignore"):
         ratio = (blocks / np.where(zero, np.float32(1), scale)[..., None]).astype(np.float32)
+    positive_nan = np.array([0x7FC00000], dtype=np.uint32).view(np.float32)[0]
+    ratio = np.where(np.isnan(ratio), positive_nan, ratio)
     q = e4m3_encode(ratio)
     q = np.where(zero[..., None], np.uint8(0), q).astype(np.uint8)
     return q.reshape(x.shape), scale

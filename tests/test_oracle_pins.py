@@ -338,6 +338,49 @@ def test_quantize_row_pins():
     check_quantize(O.quantize_row, _bf16(x))
 
 
+def test_quantize_row_non_finite_blocks():
+    """Reading R16, pinned by IEEE closed forms: a NaN anywhere in a block
+    makes its amax and scale NaN and every byte the NaN code 0x7F; an
+    infinite amax gives scale +inf, finite elements divide to a signed zero
+    (0x00 / 0x80) and infinite ones to NaN (0x7F).  Other blocks of the row
+    are quantised as if the non-finite block were not there."""
+    rng = np.random.default_rng(11)
+    x = rng.normal(0, 1, (6, 512)).astype(np.float32)
+    x[0, 5] = np.nan
+    x[1, 130] = -np.nan
+    x[1, 131] = np.inf
+    x[2, 260] = np.inf
+    x[3, 400] = -np.inf
+    x[3, 401] = np.inf
+    x[4, :128] = np.inf
+    x[5, 256:384] = np.nan
+    q, s = O.quantize_row(_bf16(x))
+    nan_blocks = [(0, 0), (1, 1), (5, 2)]
+    inf_blocks = [(2, 2), (3, 3), (4, 0)]
+    for r, j in nan_blocks:
+        assert np.isnan(s[r, j])
+        assert np.all(q[r, 128 * j:128 * (j + 1)] == 0x7F)
+    for r, j in inf_blocks:
+        assert s[r, j] == np.inf
+        blk = x[r, 128 * j:128 * (j + 1)]
+        qb = q[r, 128 * j:128 * (j + 1)]
+        fin = np.isfinite(blk)
+        assert np.all(qb[~fin] == 0x7F)
+        assert np.array_equal(qb[fin], np.where(np.signbit(blk[fin]), 0x80, 0x00))
+    # the finite blocks match the quantisation of the row with the
+    # non-finite blocks zeroed
+    xz = x.copy()
+    for r, j in nan_blocks + inf_blocks:
+        xz[r, 128 * j:128 * (j + 1)] = 0.0
+    qz, sz = O.quantize_row(_bf16(xz))
+    keep = np.ones((6, 4), bool)
+    for r, j in nan_blocks + inf_blocks:
+        keep[r, j] = False
+    assert np.array_equal(s[keep], sz[keep])
+    qk = q.reshape(6, 4, 128)[keep]
+    assert np.array_equal(qk, qz.reshape(6, 4, 128)[keep])
+
+
 # ---------------------------------------------------------------------------
 # Dispatch: identity of the copy, per-row metadata, padding
 # ---------------------------------------------------------------------------

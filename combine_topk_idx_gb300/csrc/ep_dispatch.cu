@@ -276,18 +276,24 @@ __global__ void __launch_bounds__(kMaxConsumers + 32, 1) dispatch_kernel(Dispatc
           f[2] = bf16_lo(x8.y); f[3] = bf16_hi(x8.y);
           f[4] = bf16_lo(x8.z); f[5] = bf16_hi(x8.z);
           f[6] = bf16_lo(x8.w); f[7] = bf16_hi(x8.w);
+          // amax propagates NaN (max.NaN): a block holding a NaN gets a NaN
+          // scale and the NaN code 0x7F in every byte
           float amax = 0.f;
 #pragma unroll
-          for (int q = 0; q < 8; ++q) amax = fmaxf(amax, fabsf(f[q]));
+          for (int q = 0; q < 8; ++q) amax = fmax_nan(amax, fabsf(f[q]));
           // 16 consecutive lanes hold one 128-element block
-          amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, 1));
-          amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, 2));
-          amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, 4));
-          amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, 8));
+          amax = fmax_nan(amax, __shfl_xor_sync(0xffffffffu, amax, 1));
+          amax = fmax_nan(amax, __shfl_xor_sync(0xffffffffu, amax, 2));
+          amax = fmax_nan(amax, __shfl_xor_sync(0xffffffffu, amax, 4));
+          amax = fmax_nan(amax, __shfl_xor_sync(0xffffffffu, amax, 8));
           if (valid) {
             const float sc = __fdiv_rn(amax, 448.0f);
             uint2 packed = make_uint2(0, 0);
-            if (amax != 0.f) {
+            if (amax != amax) {
+              packed = make_uint2(0x7F7F7F7Fu, 0x7F7F7F7Fu);
+            } else if (amax != 0.f) {
+              // an infinite amax: finite elements divide to +-0, infinite ones
+              // to NaN, which the conversion encodes as 0x7F
               float g[8];
 #pragma unroll
               for (int q = 0; q < 8; ++q) g[q] = __fdiv_rn(f[q], sc);

@@ -115,6 +115,13 @@ __device__ __forceinline__ uint64_t bf16x2_to_f32x2(uint32_t w) {
   return f32x2_pack(bf16_lo(w), bf16_hi(w));
 }
 
+// Maximum that returns NaN when either operand is NaN (fmaxf drops it).
+__device__ __forceinline__ float fmax_nan(float a, float b) {
+  float r;
+  asm("max.NaN.f32 %0, %1, %2;" : "=f"(r) : "f"(a), "f"(b));
+  return r;
+}
+
 __device__ __forceinline__ uint32_t lanemask_lt() {
   uint32_t r;
   asm("mov.u32 %0, %%lanemask_lt;" : "=r"(r));

@@ -187,7 +187,10 @@ EP_API ep_status ep_layout(const ep_config *cfg, const void *topk_idx, ep_stream
  *   use_tma_aligned_col_major_sf, column-major with hidden stride
  *   align(rows_alloc, 4).  scale = amax / 448 per 1x128 block (fp32 IEEE
  *   division), payload = e4m3(x / scale) round-to-nearest-even, saturating;
- *   an all-zero block has scale 0 and zero bytes.
+ *   an all-zero block has scale 0 and zero bytes.  Non-finite inputs: a
+ *   block holding a NaN gets a NaN scale and 0x7F (the e4m3 NaN code) in
+ *   every byte; a block whose amax is infinite gets scale +inf, signed
+ *   zeros for its finite elements and 0x7F for its infinite ones.
  * recv_topk_weights: NULL, or fp32 [rows_alloc] (expanded) / [rows_alloc, K]
  *   (rank layout: the token's weights on that rank, 0 elsewhere).
  * recv_topk_idx: NULL, or (rank layout only) int32 [rows_alloc, K]: the local
@@ -198,7 +201,9 @@ EP_API ep_status ep_layout(const ep_config *cfg, const void *topk_idx, ep_stream
  *   caller's own event).  May be called again with new x (cached dispatch);
  *   dispatches on one handle (this call, ep_dispatch_fp8, ep_combine_backward)
  *   must not overlap on the GPU: they share the handle's scheduling and
- *   scale-gather counters.
+ *   scale-gather counters.  A dispatch whose bounded device wait gave up
+ *   (EP_ERRBIT_TIMEOUT in the handle's error word) may leave those counters
+ *   set: free such a handle and lay out again instead of dispatching on it.
  */
 EP_API ep_status ep_dispatch(ep_handle *h, const void *x, const float *topk_weights,
                       void *recv_x, float *recv_sf, float *recv_topk_weights,
@@ -336,9 +341,11 @@ typedef struct ep_layout_buffers {
  * 256), is rejected with EP_ERR_UNSUPPORTED before any GPU work;
  * cfg->do_cpu_sync = 1 is rejected with EP_ERR_INVALID_ARG.
  *
- * The first call on a device looks up the array's device address (once per
- * device, with that device current); make that first call before any stream
- * capture.  Every call uses the same array and leaves its last contents
+ * The first call on a device looks up the array's device address (with that
+ * device current); make that first call before any stream capture.  Calls
+ * made outside a capture look the address up again (so a context re-created
+ * after cudaDeviceReset is served); calls inside a capture reuse the address
+ * of the last call outside one.  Every call uses the same array and leaves its last contents
  * there; every word a call reads is written by the same call first, so
  * nothing has to be cleared between calls.  Calls that overlap on the GPU
  * (concurrent streams, or several host threads) race on the array: order

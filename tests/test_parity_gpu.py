@@ -222,6 +222,45 @@ def test_fp8_special_values(ep):
     run_and_check(ep, cfg, idx, xf.to(torch.bfloat16), w)
 
 
+@pytest.mark.parametrize("col_major", [False, True])
+def test_fp8_non_finite_inputs(ep, col_major):
+    """NaN and +-Inf activations (reading R16): a block holding a NaN gets a
+    NaN scale and 0x7F in every byte; a block whose amax is infinite gets
+    scale +inf, signed zeros for its finite elements and 0x7F for its
+    infinite ones.  Bytes compared exactly with the oracle, scales with NaN
+    equal to NaN; the other blocks are unaffected."""
+    T, K, E, R, H = 12, 2, 4, 2, 512
+    idx = torch.tensor([[0, 3]] * T, dtype=torch.int64)
+    w = torch.full((T, K), 0.5)
+    xf = torch.randn(T, H, generator=torch.Generator().manual_seed(2))
+    xf[0, 5] = float("nan")
+    xf[1, 130] = -float("nan")
+    xf[1, 131] = float("inf")
+    xf[2, 260] = float("inf")
+    xf[3, 400] = -float("inf")
+    xf[3, 401] = float("inf")
+    xf[4, :128] = float("inf")
+    xf[5, 256:384] = float("nan")
+    xf[6, :] = -float("inf")
+    xf[7, 0] = float("nan")
+    xf[7, 128] = float("inf")
+    xf[7, 256] = -float("inf")
+    cfg = ep.make_config(T, K, E, R, H, 8, 4, True, True, True, True, col_major)
+    dev = torch.device("cuda")
+    h = ep.ep_layout(cfg, idx.to(dev))
+    lay = HN.oracle_layout(cfg, idx.numpy())
+    HN.check_layout(h, lay)
+    out = ep.alloc_recv(h, with_weights=True)
+    x = xf.to(torch.bfloat16)
+    ep.ep_dispatch(h, x.to(dev), w.to(dev), **out)
+    d_or = O.dispatch(lay, HN.bits16(x), w.numpy(), True, col_major, True)
+    HN.check_dispatch(h, lay, d_or, out, True, col_major)
+    q, s = O.quantize_row(HN.bits16(x))
+    assert np.isnan(s[0, 0]) and np.all(q[0, :128] == 0x7F)
+    assert s[4, 0] == np.inf and np.all(q[4, :128] == 0x7F)
+    h.free()
+
+
 def test_bad_topk_idx_values(ep):
     T, K, E, R, H, M = 40, 3, 8, 2, 128, 20
     idx, w = _routing(T, K, E, seed=12)

@@ -19,13 +19,17 @@ namespace {
 // [chunks] error bits.  Held by every GPU that loads the library.
 static __device__ __align__(256) int32_t g_layout_scratch[EP_NOALLOC_SCRATCH_WORDS];
 
-// Device address of g_layout_scratch, looked up once per device.
-ep_status scratch_address(int device, int32_t **out) {
+// Device address of g_layout_scratch on `device` (current).  Looked up again
+// on every call made outside a stream capture, so a context re-created after
+// cudaDeviceReset gets its own address; inside a capture the address from
+// the last call outside one is used (the first call on a device must
+// therefore come before any capture).
+ep_status scratch_address(int device, bool capturing, int32_t **out) {
   static std::mutex mu;
   static std::vector<int32_t *> addr;
   std::lock_guard<std::mutex> g(mu);
   if ((int)addr.size() <= device) addr.resize(device + 1, nullptr);
-  if (addr[device] == nullptr) {
+  if (addr[device] == nullptr || !capturing) {
     void *ptr = nullptr;
     const cudaError_t e = cudaGetSymbolAddress(&ptr, g_layout_scratch);
     if (e != cudaSuccess || ptr == nullptr) return EP_ERR_CUDA;
@@ -84,8 +88,11 @@ extern "C" ep_status ep_layout_noalloc(const ep_config *cfg, const void *topk_id
 
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess) return EP_ERR_CUDA;
+  cudaStreamCaptureStatus cs = cudaStreamCaptureStatusNone;
+  if (cudaStreamIsCapturing(reinterpret_cast<cudaStream_t>(stream), &cs) != cudaSuccess)
+    return EP_ERR_CUDA;
   int32_t *scratch = nullptr;
-  st = scratch_address(dev, &scratch);
+  st = scratch_address(dev, cs != cudaStreamCaptureStatusNone, &scratch);
   if (st != EP_OK) return st;
   lp.blk_e = scratch;
   lp.blk_r = scratch + chunks * E;

@@ -114,25 +114,68 @@ def prequantised_bytes(wl: W.Workload, T: int, topk_idx, rows_valid: int,
 
 
 # ---------------------------------------------------------------------------
-# Clock sampling during the timed region
+# Clock sampling: one nvidia-smi sampler across every GPU section of the run
 # ---------------------------------------------------------------------------
 class ClockSampler:
-    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+    FIELDS = ("timestamp,index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
               "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
               "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+    REASONS = ("hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap")
 
-    def __init__(self, gpu_index: int):
+    def __init__(self, gpu_index: int, period_ms: int = 50):
         self.proc = None
         self.gpu = gpu_index
+        self.period_ms = period_ms
+        self.sections = []      # (name, wall start, wall end)
+        self.samples = None
 
     def start(self):
         try:
             self.proc = subprocess.Popen(
                 ["nvidia-smi", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
-                 "-lms", "100", "-i", str(self.gpu)],
+                 "-lms", str(self.period_ms), "-i", str(self.gpu)],
                 stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
         except (OSError, ValueError):
             self.proc = None
+
+    def section(self, name: str):
+        """Context manager marking the wall-clock span of one GPU section."""
+        sampler = self
+
+        class _Span:
+            def __enter__(self):
+                torch.cuda.synchronize()
+                self.t0 = time.time()
+
+            def __exit__(self, *exc):
+                torch.cuda.synchronize()
+                sampler.sections.append((name, self.t0, time.time()))
+        return _Span()
+
+    def _parse(self, out: str):
+        rows = []
+        for line in out.splitlines():
+            f = [x.strip() for x in line.split(",")]
+            if len(f) < 10:
+                continue
+            try:
+                ts = time.mktime(time.strptime(f[0].split(".")[0], "%Y/%m/%d %H:%M:%S"))
+                frac = float("0." + f[0].split(".")[1]) if "." in f[0] else 0.0
+                rows.append({"t": ts + frac, "sm": float(f[2]), "smax": float(f[3]),
+                             "power": float(f[4]),
+                             "reasons": {n for n, v in zip(self.REASONS, f[6:10])
+                                         if v.lower() == "active"}})
+            except (ValueError, IndexError):
+                continue
+        return rows
+
+    @staticmethod
+    def _summary(rows) -> dict:
+        if not rows:
+            return {"sm_mhz": None, "samples": 0}
+        sm = [r["sm"] for r in rows]
+        return {"sm_mhz": statistics.median(sm), "sm_mhz_min": min(sm), "samples": len(sm),
+                "reasons": sorted(set().union(*[r["reasons"] for r in rows]))}
 
     def stop(self) -> dict:
         if self.proc is None:
@@ -143,26 +186,20 @@ class ClockSampler:
         except subprocess.TimeoutExpired:
             self.proc.kill()
             out, _ = self.proc.communicate()
-        sm, smax, reasons, power = [], [], set(), []
-        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
-        for line in out.splitlines():
-            f = [x.strip() for x in line.split(",")]
-            if len(f) < 9:
-                continue
-            try:
-                sm.append(float(f[1]))
-                smax.append(float(f[2]))
-                power.append(float(f[3]))
-            except ValueError:
-                continue
-            for n, v in zip(names, f[5:9]):
-                if v.lower() == "active":
-                    reasons.add(n)
-        if not sm:
+        rows = self._parse(out)
+        if not rows:
             return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["no samples"]}
-        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(smax),
-                "reasons": sorted(reasons), "samples": len(sm),
-                "power_w_max": max(power) if power else None}
+        inside = [r for r in rows if any(a <= r["t"] <= b for _, a, b in self.sections)]
+        use = inside or rows
+        res = self._summary(use)
+        res.update({"sm_max_mhz": max(r["smax"] for r in rows),
+                    "power_w_max": max(r["power"] for r in use),
+                    "period_ms": self.period_ms,
+                    "over": "every measured GPU section" if inside else "the whole run",
+                    "sections": {}})
+        for name, a, b in self.sections:
+            res["sections"][name] = self._summary([r for r in rows if a <= r["t"] <= b])
+        return res
 
 
 # ---------------------------------------------------------------------------
@@ -360,141 +397,285 @@ def bytes_from_layout(wl, T, topk_idx, lay: dict) -> dict:
 # ---------------------------------------------------------------------------
 # GPU arm
 # ---------------------------------------------------------------------------
+GATE_CYCLES = 2_000_000   # ~1 ms spin: the host enqueues the timed launches behind it
+L2_BYTES = 126 << 20      # GB300 L2; inputs re-read by repeated launches rotate past it
+
+# Kernels each stage launches (ours): layout = count + assign; dispatch = copy
+# kernel (+ the column-major scale gather for FP8); combine = one kernel.
+def launches(wl: W.Workload, rows_alloc: int, T: int) -> dict:
+    return {"layout": 2,
+            "dispatch": (1 + int(wl.use_fp8 and wl.col_major_sf)) if rows_alloc > 0 else 0,
+            "combine": 1 if T > 0 else 0}
+
+
+class GpuWorkload:
+    """One workload resident in HBM: inputs, the library config, expert
+    outputs y for combine (identity experts: the dequantised or copied
+    dispatch output, made once, untimed, by torch ops outside the path), the
+    algorithmic bytes of each stage, and the timed loops."""
+
+    def __init__(self, ep, wl: W.Workload, dev, seed: int, stream, flush_l2):
+        self.ep, self.wl, self.dev, self.stream, self.flush_l2 = ep, wl, dev, stream, flush_l2
+        T, H = wl.num_tokens, wl.hidden
+        self.T, self.H = T, H
+        inp = W.make_inputs(wl, seed=seed)
+        self.idx_h, self.w_h, self.x_h = inp["topk_idx"], inp["topk_weights"], inp["x"]
+        self.idx, self.w, self.x = self.idx_h.to(dev), self.w_h.to(dev), self.x_h.to(dev)
+        self.eb = inp["expert_bias"].to(dev) if inp["expert_bias"] is not None else None
+        self.cfg = ep.make_config(T, wl.num_topk, wl.num_experts, wl.num_ranks, H,
+                                  wl.num_max_tokens_per_rank, wl.expert_alignment, wl.do_expand,
+                                  wl.do_zero_padding, wl.do_cpu_sync, wl.use_fp8, wl.col_major_sf,
+                                  fixed_capacity=wl.fixed_capacity)
+        h0 = ep.ep_layout(self.cfg, self.idx)
+        out0 = ep.alloc_recv(h0, with_weights=True, with_idx=True, zero=True)
+        ep.ep_dispatch(h0, self.x, self.w, **out0)
+        rows = h0.rows_alloc
+        if wl.use_fp8:
+            q = out0["recv_x"].view(torch.float8_e4m3fn).float()
+            nb = H // 128
+            sf = out0["recv_sf"]
+            if wl.fixed_capacity and wl.col_major_sf:
+                cap = wl.num_max_tokens_per_rank * wl.num_ranks
+                st = -(-cap // 4) * 4
+                s_ = sf.view(wl.num_experts, nb, st)[:, :, :cap].permute(0, 2, 1).reshape(rows, nb)
+            elif wl.col_major_sf:
+                s_ = sf.view(nb, -1)[:, :rows].t()
+            else:
+                s_ = sf.view(rows, nb)
+            self.y = (q.view(rows, nb, 128) * s_.unsqueeze(-1)).view(rows, H).to(torch.bfloat16)
+            del q
+        else:
+            self.y = out0["recv_x"].clone()
+        g0 = {n: h0.tensor(n).cpu() for n in ("dst_buffer_slot_idx", "cnt_expert",
+                                                "cnt_expert_aligned", "totals")}
+        torch.cuda.synchronize()
+        dst = g0["dst_buffer_slot_idx"]
+        self.pad_rows = int((g0["cnt_expert_aligned"] - g0["cnt_expert"]).sum()) \
+            if wl.do_expand else 0
+        total_rows = int(g0["totals"][1] if wl.do_expand else g0["totals"][0])
+        self.valid_rows = total_rows - self.pad_rows
+        self.distinct = int(torch.unique(dst[dst >= 0]).numel())
+        self.by = stage_bytes(wl, T, self.idx_h, self.valid_rows, self.pad_rows, self.distinct,
+                              expert_bias=self.eb is not None)
+        self.out_comb = torch.empty((T, H), dtype=torch.bfloat16, device=dev)
+        self.grad_recv_w = out0["recv_topk_weights"].clone()
+        self.rows_alloc = rows
+        self.n_launch = launches(wl, rows, T)
+        h0.free()
+        del out0
+
+    def _gate(self):
+        torch.cuda._sleep(GATE_CYCLES)
+
+    def step(self, ev=None):
+        """One back-to-back step: layout -> dispatch -> combine, nothing
+        between them on the device.  ev (5 events): layout start / end,
+        dispatch start, dispatch end = combine start, combine end.  Without
+        the count wait every launch is enqueued behind a spin kernel, so no
+        host code runs inside a timed interval; with it the host waits for
+        the counts (the layout interval includes that reaction, as it does
+        for every caller of the exact allocation) and the dispatch and
+        combine launches are enqueued behind the spin kernel."""
+        ep, sync = self.ep, bool(self.cfg.do_cpu_sync)
+        if not sync:
+            self._gate()
+        if ev:
+            ev[0].record(self.stream)
+        h = ep.ep_layout(self.cfg, self.idx)
+        if ev:
+            ev[1].record(self.stream)
+        out = ep.alloc_recv(h, with_weights=True, with_idx=True)
+        if sync:
+            self._gate()
+        if ev:
+            ev[2].record(self.stream)
+        ep.ep_dispatch(h, self.x, self.w, **out)
+        if ev:
+            ev[3].record(self.stream)
+        ep.ep_combine(h, self.y, self.w, None, None, self.eb, out=self.out_comb)
+        if ev:
+            ev[4].record(self.stream)
+        h.free()
+
+    def step_flushed(self, ev=None):
+        """The same step with an L2 flush (untimed) before every stage: each
+        stage starts from a cold L2 holding no dirty lines, so the write-back
+        of what a stage leaves dirty falls in the next, untimed flush."""
+        ep = self.ep
+        self.flush_l2()
+        if ev:
+            ev[0].record(self.stream)
+        h = ep.ep_layout(self.cfg, self.idx)
+        if ev:
+            ev[1].record(self.stream)
+        out = ep.alloc_recv(h, with_weights=True, with_idx=True)
+        self.flush_l2()
+        if ev:
+            ev[2].record(self.stream)
+        ep.ep_dispatch(h, self.x, self.w, **out)
+        if ev:
+            ev[3].record(self.stream)
+        self.flush_l2()
+        if ev:
+            ev[4].record(self.stream)
+        ep.ep_combine(h, self.y, self.w, None, None, self.eb, out=self.out_comb)
+        if ev:
+            ev[5].record(self.stream)
+        h.free()
+
+    def run_steps(self, n: int, warmup: int, flushed: bool = False) -> dict:
+        """Warm-up, then n steps with the L2 flushed between steps; returns the
+        mean per-stage device times (ms)."""
+        fn = self.step_flushed if flushed else self.step
+        for _ in range(warmup):
+            if not flushed:
+                self.flush_l2()
+            fn()
+        torch.cuda.synchronize()
+        nev = 6 if flushed else 5
+        evs = [[torch.cuda.Event(enable_timing=True) for _ in range(nev)] for _ in range(n)]
+        for i in range(n):
+            if not flushed:
+                self.flush_l2()
+            fn(evs[i])
+        torch.cuda.synchronize()
+        if flushed:
+            lay = [e[0].elapsed_time(e[1]) for e in evs]
+            dis = [e[2].elapsed_time(e[3]) for e in evs]
+            com = [e[4].elapsed_time(e[5]) for e in evs]
+        else:
+            lay = [e[0].elapsed_time(e[1]) for e in evs]
+            dis = [e[2].elapsed_time(e[3]) for e in evs]
+            com = [e[3].elapsed_time(e[4]) for e in evs]
+        return {"layout": statistics.mean(lay), "dispatch": statistics.mean(dis),
+                "combine": statistics.mean(com),
+                "step": statistics.mean(a + b + c for a, b, c in zip(lay, dis, com)),
+                "launches": n * sum(self.n_launch.values())}
+
+    def stage_block(self, t: dict, peak: float) -> dict:
+        out = {}
+        for k in ("layout", "dispatch", "combine"):
+            gbs = self.by[k] / t[k] / 1e6
+            out[k] = {"ms": round(t[k], 5), "bytes": self.by[k], "gbs": round(gbs, 1)}
+            if k != "layout":
+                out[k]["frac_of_peak"] = round(gbs / peak, 4)
+        tot = sum(self.by.values())
+        out["step"] = {"ms": round(t["step"], 5), "bytes": tot,
+                       "gbs": round(tot / t["step"] / 1e6, 1),
+                       "frac_of_peak": round(tot / t["step"] / 1e6 / peak, 4),
+                       "tokens_per_s": round(self.T / (t["step"] * 1e-3), 1)}
+        return out
+
+    def _copies(self, t: torch.Tensor) -> list:
+        """t and enough clones that cycling through them re-reads more than
+        twice the L2 between two uses of one copy."""
+        n = max(1, min(4, -(-2 * L2_BYTES // max(1, t.numel() * t.element_size()))))
+        return [t] + [t.clone() for _ in range(n - 1)]
+
+    def sustained(self, n: int, peak: float) -> dict:
+        """Dispatch alone, then combine alone, launched n times back to back
+        behind a spin kernel: each launch pays the write-back of the lines the
+        launch before it left dirty, i.e. in steady state its own.  Inputs
+        rotate over copies that together exceed the L2."""
+        ep = self.ep
+        h = ep.ep_layout(self.cfg, self.idx)
+        out = ep.alloc_recv(h, with_weights=True, with_idx=True)
+        xs = self._copies(self.x)
+        ys = self._copies(self.y)
+        res = {}
+        for name in ("dispatch", "combine"):
+            def launch(i):
+                if name == "dispatch":
+                    ep.ep_dispatch(h, xs[i % len(xs)], self.w, **out)
+                else:
+                    ep.ep_combine(h, ys[i % len(ys)], self.w, None, None, self.eb,
+                                  out=self.out_comb)
+            for i in range(3):
+                launch(i)
+            self.flush_l2()
+            self._gate()
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            e0.record(self.stream)
+            for i in range(n):
+                launch(i)
+            e1.record(self.stream)
+            torch.cuda.synchronize()
+            ms = e0.elapsed_time(e1) / n
+            gbs = self.by[name] / ms / 1e6
+            res[name] = {"ms": round(ms, 5), "gbs": round(gbs, 1),
+                         "frac_of_peak": round(gbs / peak, 4), "launches": n,
+                         "input_copies": len(xs) if name == "dispatch" else len(ys)}
+        h.free()
+        del xs, ys
+        return res
+
+
 def run_gpu(args, ws, rank, local):
-    import numpy as np
     import combine_topk_idx_gb300 as ep
 
     torch.cuda.set_device(local)
     dev = torch.device("cuda", local)
     init_dist(ws, "nccl")
     ep.load_library()
-    wl = W.WORKLOADS[args.workload]
-    T, H = wl.num_tokens, wl.hidden
-    inp = W.make_inputs(wl, seed=args.seed)
-    idx_h, w_h, x_h = inp["topk_idx"], inp["topk_weights"], inp["x"]
-    idx, w, x = idx_h.to(dev), w_h.to(dev), x_h.to(dev)
-    eb = inp["expert_bias"].to(dev) if inp["expert_bias"] is not None else None
-    cfg = ep.make_config(T, wl.num_topk, wl.num_experts, wl.num_ranks, H,
-                         wl.num_max_tokens_per_rank, wl.expert_alignment, wl.do_expand,
-                         wl.do_zero_padding, wl.do_cpu_sync, wl.use_fp8, wl.col_major_sf,
-                         fixed_capacity=wl.fixed_capacity)
+    peaks = load_peaks()
+    peak = peaks["hbm_gbs"]
     stream = torch.cuda.current_stream()
     flush_w = torch.empty(L2_FLUSH_BYTES // 4, dtype=torch.float32, device=dev)
     flush_r = torch.ones(L2_FLUSH_BYTES // 4, dtype=torch.float32, device=dev)
 
     def flush_l2():
         # write a buffer larger than L2, then read another one, so that the
-        # next timed stage starts with a cold L2 holding no dirty lines
+        # next timed launch starts with a cold L2 holding no dirty lines
         flush_w.zero_()
         flush_r.sum()
 
-    # Expert outputs for combine (identity experts): y = dequantised / copied
-    # recv_x, produced once, untimed, by torch ops (not part of the path).
-    h0 = ep.ep_layout(cfg, idx)
-    out0 = ep.alloc_recv(h0, with_weights=True, with_idx=True, zero=True)
-    ep.ep_dispatch(h0, x, w, **out0)
-    rows = h0.rows_alloc
-    if wl.use_fp8:
-        q = out0["recv_x"].view(torch.float8_e4m3fn).float()
-        nb = H // 128
-        sf = out0["recv_sf"]
-        if wl.col_major_sf:
-            s = sf.view(nb, -1)[:, :rows].t()
-        else:
-            s = sf.view(rows, nb)
-        y = (q.view(rows, nb, 128) * s.unsqueeze(-1)).view(rows, H).to(torch.bfloat16)
-        del q
-    else:
-        y = out0["recv_x"].clone()
-    g0 = {n: h0.tensor(n).cpu() for n in ("dst_buffer_slot_idx", "cnt_expert",
-                                            "cnt_expert_aligned", "totals")}
-    torch.cuda.synchronize()
-    dst = g0["dst_buffer_slot_idx"]
-    pad_rows = int((g0["cnt_expert_aligned"] - g0["cnt_expert"]).sum()) if wl.do_expand else 0
-    total_rows = int(g0["totals"][1] if wl.do_expand else g0["totals"][0])
-    valid_rows = total_rows - pad_rows
-    distinct = int(torch.unique(dst[dst >= 0]).numel())
-    by = stage_bytes(wl, T, idx_h, valid_rows, pad_rows, distinct,
-                     expert_bias=eb is not None)
-    out_comb = torch.empty((T, H), dtype=torch.bfloat16, device=dev)
-    grad_recv_w = out0["recv_topk_weights"].clone()
-    h0.free()
-    del out0
-
-    def one_step(timed: bool, ev=None, flush=True):
-        if flush:
-            flush_l2()
-        if timed:
-            ev[0].record(stream)
-        h = ep.ep_layout(cfg, idx)
-        if timed:
-            ev[1].record(stream)
-        out = ep.alloc_recv(h, with_weights=True, with_idx=True)
-        if flush:
-            flush_l2()
-        if timed:
-            ev[2].record(stream)
-        ep.ep_dispatch(h, x, w, **out)
-        if timed:
-            ev[3].record(stream)
-        if flush:
-            flush_l2()
-        if timed:
-            ev[4].record(stream)
-        ep.ep_combine(h, y, w, None, None, eb, out=out_comb)
-        if timed:
-            ev[5].record(stream)
-        h.free()
-        return h.rows_alloc
-
-    for _ in range(args.warmup):
-        one_step(False)
-    torch.cuda.synchronize()
-    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(6)] for _ in range(args.steps)]
     clocks = ClockSampler(local)
     clocks.start()
     time.sleep(0.25)
-    barrier(ws)
+    wl = W.WORKLOADS[args.workload]
+    main = GpuWorkload(ep, wl, dev, args.seed, stream, flush_l2)
+    T, H = main.T, main.H
+    by = main.by
+    total_bytes = sum(by.values())
+
+    # ---- the timed steps: back to back, L2 flushed between steps ----
+    for _ in range(args.warmup):
+        flush_l2()
+        main.step()
     torch.cuda.synchronize()
-    launches = 0
-    for i in range(args.steps):
-        r = one_step(True, evs[i])
-        # layout: count + assign; dispatch: the copy kernel (+ the column-major
-        # scale gather for FP8); combine: one kernel
-        launches += 2 + ((1 + int(wl.use_fp8 and wl.col_major_sf)) if r > 0 else 0) + \
-            (1 if T > 0 else 0)
-    torch.cuda.synchronize()
+    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(5)] for _ in range(args.steps)]
     barrier(ws)
-    clk = clocks.stop()
+    with clocks.section("timed_steps"):
+        for i in range(args.steps):
+            flush_l2()
+            main.step(evs[i])
+    barrier(ws)
     lay_ms = [e[0].elapsed_time(e[1]) for e in evs]
     dis_ms = [e[2].elapsed_time(e[3]) for e in evs]
-    com_ms = [e[4].elapsed_time(e[5]) for e in evs]
+    com_ms = [e[3].elapsed_time(e[4]) for e in evs]
     step_ms = statistics.mean(a + b + c for a, b, c in zip(lay_ms, dis_ms, com_ms))
     step_ms_max = max_over_ranks(step_ms, ws, dev)
-    total_bytes = sum(by.values())
     value = total_bytes * ws / (step_ms_max * 1e-3) / 1e9
+    n_launch = args.steps * sum(main.n_launch.values())
+    t_main = {"layout": statistics.mean(lay_ms), "dispatch": statistics.mean(dis_ms),
+              "combine": statistics.mean(com_ms), "step": step_ms}
 
-    # Secondary: warm L2 (no flush between stages), same step, untimed warm-up.
-    warm_steps = max(8, args.steps // 8)
-    for _ in range(3):
-        one_step(False, flush=False)
-    wev = [[torch.cuda.Event(enable_timing=True) for _ in range(6)] for _ in range(warm_steps)]
-    torch.cuda.synchronize()
-    for i in range(warm_steps):
-        one_step(True, wev[i], flush=False)
-    torch.cuda.synchronize()
-    warm = {k: statistics.mean(e[a].elapsed_time(e[b]) for e in wev)
-            for k, a, b in (("layout", 0, 1), ("dispatch", 2, 3), ("combine", 4, 5))}
+    # ---- secondary figures on the same workload ----
+    fl_steps = max(8, args.steps // 2)
+    with clocks.section("stages_flushed"):
+        t_fl = main.run_steps(fl_steps, 3, flushed=True)
+    with clocks.section("sustained"):
+        sus = main.sustained(max(10, args.steps // 2), peak)
     # Host wall time of the layout call on an idle GPU (with do_cpu_sync it
     # includes the count wait).
     layout_host_s = []
-    for _ in range(20):
-        torch.cuda.synchronize()
-        t_host = time.perf_counter()
-        h = ep.ep_layout(cfg, idx)
-        layout_host_s.append(time.perf_counter() - t_host)
-        h.free()
-    torch.cuda.synchronize()
+    with clocks.section("layout_host"):
+        for _ in range(20):
+            torch.cuda.synchronize()
+            t_host = time.perf_counter()
+            h = ep.ep_layout(main.cfg, main.idx)
+            layout_host_s.append(time.perf_counter() - t_host)
+            h.free()
 
     # e2e through the C ABI with host buffers: every step copies its inputs
     # (topk_idx, topk_weights, x) in from pinned host memory and its combined
@@ -502,10 +683,11 @@ def run_gpu(args, ws, rank, local):
     # the next step's input copies are enqueued before this step's layout
     # (whose count wait blocks the host), so one step's copies overlap the
     # neighbouring steps' kernels and copies, as a serving loop would run them.
-    idx_pin, w_pin, x_pin = idx_h.pin_memory(), w_h.pin_memory(), x_h.pin_memory()
+    idx_pin, w_pin, x_pin = main.idx_h.pin_memory(), main.w_h.pin_memory(), main.x_h.pin_memory()
     nbuf = 3
     e2e_streams = [torch.cuda.Stream(device=dev) for _ in range(nbuf)]
-    e2e_bufs = [{"idx": torch.empty_like(idx), "w": torch.empty_like(w), "x": torch.empty_like(x),
+    e2e_bufs = [{"idx": torch.empty_like(main.idx), "w": torch.empty_like(main.w),
+                 "x": torch.empty_like(main.x),
                  "out": torch.empty((T, H), dtype=torch.bfloat16, device=dev),
                  "out_pin": torch.empty((T, H), dtype=torch.bfloat16).pin_memory()}
                 for _ in range(nbuf)]
@@ -521,10 +703,10 @@ def run_gpu(args, ws, rank, local):
         st = e2e_streams[i % nbuf]
         b = e2e_bufs[i % nbuf]
         with torch.cuda.stream(st):
-            h = ep.ep_layout(cfg, b["idx"], stream=st)
+            h = ep.ep_layout(main.cfg, b["idx"], stream=st)
             out = ep.alloc_recv(h, with_weights=True, with_idx=True)
             ep.ep_dispatch(h, b["x"], b["w"], **out, stream=st)
-            ep.ep_combine(h, y, b["w"], None, None, eb, out=b["out"], stream=st)
+            ep.ep_combine(h, main.y, b["w"], None, None, main.eb, out=b["out"], stream=st)
             b["out_pin"].copy_(b["out"], non_blocking=True)
             h.free()
 
@@ -543,20 +725,20 @@ def run_gpu(args, ws, rank, local):
     torch.cuda.synchronize()
     e2e_steps = max(8, args.steps // 4)
     barrier(ws)
-    e_s, e_e = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    flush_l2()
-    e_s.record(stream)
-    e2e_run(e2e_steps)
-    e_e.record(stream)
-    torch.cuda.synchronize()
+    with clocks.section("e2e"):
+        e_s, e_e = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        flush_l2()
+        e_s.record(stream)
+        e2e_run(e2e_steps)
+        e_e.record(stream)
     e2e_ms = max_over_ranks(e_s.elapsed_time(e_e) / e2e_steps, ws, dev)
     barrier(ws)
 
     # Backward pair on one handle (layout untimed): combine_backward dispatches
     # a [T, H] gradient, dispatch_backward combines a [rows, H] gradient and
     # reduces the weight gradients.  L2 is flushed before each timed call.
-    bwd_by = backward_bytes(wl, T, idx_h, valid_rows, pad_rows, distinct)
-    hb = ep.ep_layout(cfg, idx)
+    bwd_by = backward_bytes(wl, T, main.idx_h, main.valid_rows, main.pad_rows, main.distinct)
+    hb = ep.ep_layout(main.cfg, main.idx)
     g_recv = torch.empty((hb.rows_alloc, H), dtype=torch.bfloat16, device=dev)
     g_x = torch.empty((T, H), dtype=torch.bfloat16, device=dev)
     g_w = torch.empty((T, wl.num_topk), dtype=torch.float32, device=dev)
@@ -565,13 +747,13 @@ def run_gpu(args, ws, rank, local):
         flush_l2()
         if ev:
             ev[0].record(stream)
-        ep.ep_combine_backward(hb, x, g_recv)
+        ep.ep_combine_backward(hb, main.x, g_recv)
         if ev:
             ev[1].record(stream)
         flush_l2()
         if ev:
             ev[2].record(stream)
-        ep.ep_dispatch_backward(hb, y, grad_recv_w, g_x, g_w)
+        ep.ep_dispatch_backward(hb, main.y, main.grad_recv_w, g_x, g_w)
         if ev:
             ev[3].record(stream)
 
@@ -579,10 +761,9 @@ def run_gpu(args, ws, rank, local):
         bwd_step()
     bwd_steps = max(8, args.steps // 4)
     bev = [[torch.cuda.Event(enable_timing=True) for _ in range(4)] for _ in range(bwd_steps)]
-    torch.cuda.synchronize()
-    for i in range(bwd_steps):
-        bwd_step(bev[i])
-    torch.cuda.synchronize()
+    with clocks.section("backward"):
+        for i in range(bwd_steps):
+            bwd_step(bev[i])
     cb_ms = statistics.mean(e[0].elapsed_time(e[1]) for e in bev)
     db_ms = statistics.mean(e[2].elapsed_time(e[3]) for e in bev)
     del g_recv, g_x, g_w
@@ -592,7 +773,7 @@ def run_gpu(args, ws, rank, local):
     pq = None
     if wl.use_fp8:
         nb = H // 128
-        xb = x.float().view(T, nb, 128)
+        xb = main.x.float().view(T, nb, 128)
         sc = xb.abs().amax(-1) / 448.0
         sc = torch.where(sc > 0, sc, torch.ones_like(sc))
         xq = (xb / sc.unsqueeze(-1)).to(torch.float8_e4m3fn).view(T, H)
@@ -602,37 +783,66 @@ def run_gpu(args, ws, rank, local):
         xs = sf_store[:, :T].t()
         del xb
         pq_out = ep.alloc_recv(hb, with_weights=True, with_idx=True)
-        pq_by = prequantised_bytes(wl, T, idx_h, valid_rows, pad_rows)
+        pq_by = prequantised_bytes(wl, T, main.idx_h, main.valid_rows, main.pad_rows)
 
         def pq_step(ev=None):
             flush_l2()
             if ev:
                 ev[0].record(stream)
-            ep.ep_dispatch_fp8(hb, xq, xs, w, **pq_out)
+            ep.ep_dispatch_fp8(hb, xq, xs, main.w, **pq_out)
             if ev:
                 ev[1].record(stream)
 
         for _ in range(args.warmup):
             pq_step()
         pev = [[torch.cuda.Event(enable_timing=True) for _ in range(2)] for _ in range(bwd_steps)]
-        torch.cuda.synchronize()
-        for i in range(bwd_steps):
-            pq_step(pev[i])
-        torch.cuda.synchronize()
+        with clocks.section("dispatch_prequantised"):
+            for i in range(bwd_steps):
+                pq_step(pev[i])
         pq_ms = statistics.mean(e[0].elapsed_time(e[1]) for e in pev)
         pq = {"steps": bwd_steps, "ms": round(pq_ms, 5), "bytes": pq_by,
               "gbs": round(pq_by / pq_ms / 1e6, 1),
-              "input_sf": "column-major TMA-aligned",
+              "frac_of_peak": round(pq_by / pq_ms / 1e6 / peak, 4),
+              "input_sf": "column-major TMA-aligned", "l2": "flushed before each call",
               "gpu_launches": bwd_steps * (1 + int(wl.col_major_sf))}
         del pq_out, xq, sf_store
     hb.free()
 
-    peaks = load_peaks()
-    d_ms, c_ms = statistics.mean(dis_ms), statistics.mean(com_ms)
+    # ---- every other workload: the same back-to-back step and the flushed
+    # stages, a few steps each (N = 1 only) ----
+    wl_block = {}
+    if ws == 1 and not args.no_workloads:
+        del main.y
+        for name in [n for n in ("decode", "decode_ll", "skewed", "large", "tiny")
+                     if n != wl.name]:
+            other = GpuWorkload(ep, W.WORKLOADS[name], dev, args.seed, stream, flush_l2)
+            with clocks.section(f"workload_{name}"):
+                tb = other.run_steps(args.workload_steps, 3)
+                tf = other.run_steps(args.workload_steps, 3, flushed=True)
+                su = other.sustained(args.workload_steps, peak)
+            wl_block[name] = {
+                "config": {"tokens": other.T, "hidden": other.H,
+                           "experts": other.wl.num_experts,
+                           "logical_ranks": other.wl.num_ranks, "topk": other.wl.num_topk,
+                           "do_expand": other.wl.do_expand, "fp8_dispatch": other.wl.use_fp8,
+                           "do_cpu_sync": other.wl.do_cpu_sync,
+                           "fixed_capacity": other.wl.fixed_capacity},
+                "steps": args.workload_steps,
+                "back_to_back": other.stage_block(tb, peak),
+                "stages_flushed": other.stage_block(tf, peak),
+                "sustained": su,
+                "gpu_launches": tb["launches"] + tf["launches"],
+            }
+            del other
+            torch.cuda.empty_cache()
+
+    clk = clocks.stop()
+    d_ms, c_ms = t_main["dispatch"], t_main["combine"]
     dom = "combine" if c_ms >= d_ms else "dispatch"
     dom_ms = c_ms if dom == "combine" else d_ms
     achieved = by[dom] / (dom_ms * 1e-3) / 1e9
     traffic = recorded_traffic(dom, wl.name)
+    stages = main.stage_block(t_main, peak)
     line = {
         "metric": METRIC, "value": round(value, 2), "unit": "GB/s", "n_gpus": ws,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(step_ms_max, 5),
@@ -643,56 +853,59 @@ def run_gpu(args, ws, rank, local):
                    "expert_alignment": wl.expert_alignment, "do_expand": wl.do_expand,
                    "fp8_dispatch": wl.use_fp8, "col_major_sf": wl.col_major_sf,
                    "do_cpu_sync": wl.do_cpu_sync, "routing": wl.routing,
-                   "l2": "flushed before each stage (256 MiB write, then 256 MiB read); "
-                         "times are device events",
+                   "l2": "flushed between steps (256 MiB write, then 256 MiB read); inside a "
+                         "step the stages run back to back; times are device events",
                    "parallelism": f"replicas x{ws}"},
         "tokens_per_s": round(T * ws / (step_ms_max * 1e-3), 1),
-        "pct_of_hbm_peak": round(100 * value / ws / peaks["hbm_gbs"], 2),
-        "stages": {
-            "layout": {"ms": round(statistics.mean(lay_ms), 5), "bytes": by["layout"],
-                       "gbs": round(by["layout"] / statistics.mean(lay_ms) / 1e6, 1)},
-            "dispatch": {"ms": round(d_ms, 5), "bytes": by["dispatch"],
-                         "gbs": round(by["dispatch"] / d_ms / 1e6, 1),
-                         "frac_of_peak": round(by["dispatch"] / d_ms / 1e6 / peaks["hbm_gbs"], 4)},
-            "combine": {"ms": round(c_ms, 5), "bytes": by["combine"],
-                        "gbs": round(by["combine"] / c_ms / 1e6, 1),
-                        "frac_of_peak": round(by["combine"] / c_ms / 1e6 / peaks["hbm_gbs"], 4)},
-        },
-        "layout_plus_dispatch_ms": round(statistics.mean(lay_ms) + d_ms, 5),
+        "pct_of_hbm_peak": round(100 * value / ws / peak, 2),
+        "stages": {k: v for k, v in stages.items() if k != "step"},
+        "stages_how": "one step = layout, dispatch, combine back to back on the device; the "
+                      "dispatch and combine launches are enqueued behind a spin kernel after "
+                      "the count wait, so no host code falls inside their intervals; the "
+                      "layout interval includes the host's reaction to the count wait",
+        "layout_plus_dispatch_ms": round(t_main["layout"] + d_ms, 5),
         "layout_host_ms": round(1e3 * statistics.median(layout_host_s), 5),
-        "warm_l2": {"steps": warm_steps,
-                    **{k: {"ms": round(v, 5), "gbs": round(by[k] / v / 1e6, 1)}
-                       for k, v in warm.items()}},
+        "stages_flushed": {**{k: v for k, v in main.stage_block(t_fl, peak).items()},
+                           "steps": fl_steps,
+                           "how": "L2 flushed before every stage (no dirty lines inherited; "
+                                  "a stage's own dirty lines drain in the next, untimed flush)"},
+        "sustained": {**sus, "how": "each kernel launched back to back behind a spin kernel, "
+                                    "inputs rotating over copies larger than L2: every launch "
+                                    "pays the write-back of its predecessor's dirty lines, in "
+                                    "steady state its own"},
         "roofline": {"bound": "hbm", "kernel": dom, "achieved": round(achieved, 1),
-                     "peak": peaks["hbm_gbs"], "peak_source": peaks["source"], "unit": "GB/s",
-                     "frac": round(achieved / peaks["hbm_gbs"], 4), "traffic": traffic,
-                     "algorithmic_bytes": by[dom]},
+                     "peak": peak, "peak_source": peaks["source"], "unit": "GB/s",
+                     "frac": round(achieved / peak, 4), "traffic": traffic,
+                     "algorithmic_bytes": by[dom],
+                     "sustained_frac": sus[dom]["frac_of_peak"]},
         "e2e": {"value": round(total_bytes * ws / (e2e_ms * 1e-3) / 1e9, 2), "unit": "GB/s",
                 "ms_per_step": round(e2e_ms, 5),
                 "how": "C ABI with host buffers: per step, pinned h2d of topk_idx, weights and x, "
                        "layout + dispatch + combine, d2h of the output; consecutive steps "
                        "rotate over three streams, the next step's inputs are copied in before "
                        "this step's layout (copies overlap neighbouring steps)",
-                "h2d_bytes_per_step": idx_h.numel() * 8 + w_h.numel() * 4 + x_h.numel() * 2,
+                "h2d_bytes_per_step": main.idx_h.numel() * 8 + main.w_h.numel() * 4
+                + main.x_h.numel() * 2,
                 "d2h_bytes_per_step": T * H * 2},
-        "gpu_launches": launches,
+        "gpu_launches": n_launch,
         "clocks": clk,
         "backward": {
-            "steps": bwd_steps,
+            "steps": bwd_steps, "l2": "flushed before each call",
             "combine_backward": {"ms": round(cb_ms, 5), "bytes": bwd_by["combine_backward"],
                                  "gbs": round(bwd_by["combine_backward"] / cb_ms / 1e6, 1),
                                  "frac_of_peak": round(bwd_by["combine_backward"] / cb_ms / 1e6
-                                                       / peaks["hbm_gbs"], 4)},
+                                                       / peak, 4)},
             "dispatch_backward": {"ms": round(db_ms, 5), "bytes": bwd_by["dispatch_backward"],
                                   "gbs": round(bwd_by["dispatch_backward"] / db_ms / 1e6, 1),
                                   "frac_of_peak": round(bwd_by["dispatch_backward"] / db_ms / 1e6
-                                                        / peaks["hbm_gbs"], 4)},
+                                                        / peak, 4)},
             "gpu_launches": bwd_steps * ((1 if T > 0 else 0) + (2 if T > 0 else 0)),
         },
     }
     if pq is not None:
-        pq["frac_of_peak"] = round(pq["gbs"] / peaks["hbm_gbs"], 4)
         line["dispatch_prequantised"] = pq
+    if wl_block:
+        line["workloads"] = wl_block
     if rank == 0 and ws == 1 and not args.no_cpu_baseline:
         cb = time_oracle(wl, args.cpu_sample_tokens, args.cpu_budget_s, seed=args.seed)
         line["cpu_baseline"] = {"value": round(cb["gbs"], 4), "unit": "GB/s", "cores": 1,
@@ -762,6 +975,9 @@ def main(argv=None):
     ap.add_argument("--cpu-sample-tokens", type=int, default=512)
     ap.add_argument("--cpu-budget-s", type=float, default=10.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-workloads", action="store_true",
+                    help="skip the block that times every other workload")
+    ap.add_argument("--workload-steps", type=int, default=10)
     args = ap.parse_args(argv)
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")

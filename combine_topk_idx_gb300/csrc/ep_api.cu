@@ -39,6 +39,55 @@ int device_sm_count(int device) {
   return cache[device];
 }
 
+cudaError_t launch_geometry(const void *func, int threads, size_t smem, int *device,
+                            int *per_sm) {
+  struct Entry {
+    const void *func;
+    int device, threads;
+    size_t smem;
+    int per_sm;
+  };
+  struct OptIn {
+    const void *func;
+    int device;
+    size_t smem;  // largest dynamic shared memory opted in so far
+  };
+  static std::mutex mu;
+  static std::vector<Entry> shapes;
+  static std::vector<OptIn> optins;
+  int dev = 0;
+  cudaError_t err = cudaGetDevice(&dev);
+  if (err != cudaSuccess) return err;
+  *device = dev;
+  std::lock_guard<std::mutex> g(mu);
+  if (per_sm != nullptr)
+    for (const Entry &e : shapes)
+      if (e.func == func && e.device == dev && e.threads == threads && e.smem == smem) {
+        *per_sm = e.per_sm;
+        return cudaSuccess;
+      }
+  if (smem > kDynSmemOptIn) {
+    OptIn *o = nullptr;
+    for (OptIn &x : optins)
+      if (x.func == func && x.device == dev) o = &x;
+    if (o == nullptr || o->smem < smem) {
+      err = cudaFuncSetAttribute(func, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+      if (err != cudaSuccess) return err;
+      if (o == nullptr)
+        optins.push_back({func, dev, smem});
+      else
+        o->smem = smem;
+    }
+  }
+  if (per_sm == nullptr) return cudaSuccess;  // the opt-in only
+  int n = 0;
+  err = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, func, threads, smem);
+  if (err != cudaSuccess) return err;
+  shapes.push_back({func, dev, threads, smem, n});
+  *per_sm = n;
+  return cudaSuccess;
+}
+
 namespace {
 
 inline int64_t align_up(int64_t x, int64_t a) { return (x + a - 1) / a * a; }
@@ -91,12 +140,17 @@ ep_status wait_host_words(const HostSync *slot, int32_t seq, int32_t timeout_ms,
   }
 }
 
-// Pool of pinned, device-mapped host words for the count wait.
+// Pool of pinned, device-mapped host words for the count wait.  Each slot
+// keeps the device address of its mapping, looked up once per block of slots.
 struct SyncPool {
+  struct Slot {
+    HostSync *host;
+    HostSync *dev;
+  };
   std::mutex mu;
-  std::vector<HostSync *> free_list;
+  std::vector<Slot> free_list;
   int32_t seq = 0;
-  HostSync *acquire(int32_t *seq_out) {
+  bool acquire(int32_t *seq_out, Slot *out) {
     std::lock_guard<std::mutex> g(mu);
     *seq_out = ++seq;
     if (seq > 0x3fffffff) seq = 0;
@@ -105,15 +159,21 @@ struct SyncPool {
       void *mem = nullptr;
       if (cudaHostAlloc(&mem, n * sizeof(HostSync), cudaHostAllocMapped | cudaHostAllocPortable) !=
           cudaSuccess)
-        return nullptr;
+        return false;
+      void *dmem = nullptr;
+      if (cudaHostGetDevicePointer(&dmem, mem, 0) != cudaSuccess) {
+        cudaFreeHost(mem);
+        return false;
+      }
       HostSync *s = static_cast<HostSync *>(mem);
-      for (int i = 0; i < n; ++i) free_list.push_back(s + i);
+      HostSync *d = static_cast<HostSync *>(dmem);
+      for (int i = 0; i < n; ++i) free_list.push_back({s + i, d + i});
     }
-    HostSync *h = free_list.back();
+    *out = free_list.back();
     free_list.pop_back();
-    return h;
+    return true;
   }
-  void release(HostSync *h) {
+  void release(const Slot &h) {
     std::lock_guard<std::mutex> g(mu);
     free_list.push_back(h);
   }
@@ -404,19 +464,12 @@ ep_status ep_layout(const ep_config *cfg, const void *topk_idx, ep_stream_t stre
     return code;
   };
 
-  ep::HostSync *slot = nullptr;
+  ep::SyncPool::Slot slot{nullptr, nullptr};
   if (c.do_cpu_sync) {
     int32_t seq = 0;
-    slot = ep::sync_pool().acquire(&seq);
-    if (slot == nullptr) return fail(EP_ERR_OOM);
-    slot->num_recv = slot->num_expanded = slot->error = 0;
-    void *dptr = nullptr;
-    ce = cudaHostGetDevicePointer(&dptr, (void *)slot, 0);
-    if (ce != cudaSuccess) {
-      ep::sync_pool().release(slot);
-      return fail(ep::cuda_status(ce));
-    }
-    lp.host = static_cast<ep::HostSync *>(dptr);
+    if (!ep::sync_pool().acquire(&seq, &slot)) return fail(EP_ERR_OOM);
+    slot.host->num_recv = slot.host->num_expanded = slot.host->error = 0;
+    lp.host = slot.dev;
     lp.seq = seq;
   }
   ce = ep::launch_layout(lp, s);
@@ -440,7 +493,7 @@ ep_status ep_layout(const ep_config *cfg, const void *topk_idx, ep_stream_t stre
   if (c.do_cpu_sync) {
     const int32_t timeout = c.cpu_sync_timeout_ms > 0 ? c.cpu_sync_timeout_ms : 10000;
     uint64_t words[3];
-    const ep_status w = ep::wait_host_words(slot, lp.seq, timeout, words);
+    const ep_status w = ep::wait_host_words(slot.host, lp.seq, timeout, words);
     if (w != EP_OK) {
       // the slot may still be written later: leave it out of the pool
       delete h;

@@ -293,16 +293,9 @@ cudaError_t launch_one(const CombineParams &p, int sm_cap, cudaStream_t s) {
   const int consumers = std::min(kMaxConsumers, (nv + 31) / 32 * 32);
   const int threads = consumers + 32;
   const size_t smem = (size_t)kStages * slots_cap * chunk;
-  cudaError_t err;
-  if (smem > kDynSmemOptIn) {
-    err = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-    if (err != cudaSuccess) return err;
-  }
-  int dev = 0;
-  err = cudaGetDevice(&dev);
-  if (err != cudaSuccess) return err;
-  int per_sm = 0;
-  err = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kern, threads, smem);
+  int dev = 0, per_sm = 0;
+  cudaError_t err =
+      launch_geometry(reinterpret_cast<const void *>(kern), threads, smem, &dev, &per_sm);
   if (err != cudaSuccess) return err;
   if (per_sm < 1) per_sm = 1;
   const int sms = device_sm_count(dev);

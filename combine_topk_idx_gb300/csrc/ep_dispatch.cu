@@ -516,16 +516,9 @@ cudaError_t launch_one(const DispatchParams &p0, int sm_cap, cudaStream_t s) {
     }
   }
   const size_t smem = stages * (in_stage + out_stage + sf_stage);
-  cudaError_t err;
-  if (smem > kDynSmemOptIn) {
-    err = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-    if (err != cudaSuccess) return err;
-  }
-  int dev = 0;
-  err = cudaGetDevice(&dev);
-  if (err != cudaSuccess) return err;
-  int per_sm = 0;
-  err = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kern, threads, smem);
+  int dev = 0, per_sm = 0;
+  cudaError_t err =
+      launch_geometry(reinterpret_cast<const void *>(kern), threads, smem, &dev, &per_sm);
   if (err != cudaSuccess) return err;
   if (per_sm < 1) per_sm = 1;
   const int sms = device_sm_count(dev);

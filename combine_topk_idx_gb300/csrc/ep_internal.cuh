@@ -147,4 +147,13 @@ cudaError_t launch_combine_weights(const CombineWeightsParams &p, cudaStream_t s
 // Device facts, cached per device.
 int device_sm_count(int device);
 
+// Resident CTAs per SM of `func` at (threads, dynamic shared memory) on the
+// current device, with the dynamic shared-memory opt-in (above
+// kDynSmemOptIn) applied first.  Both are looked up once per device,
+// function and shape and cached for the life of the process, so a launch
+// makes no runtime query after the first of its shape.  per_sm = nullptr
+// applies the opt-in only.
+cudaError_t launch_geometry(const void *func, int threads, size_t smem, int *device,
+                            int *per_sm);
+
 }  // namespace ep

@@ -469,17 +469,13 @@ int layout_rank_warps(int nkey) {
 cudaError_t launch_layout(const LayoutParams &p, cudaStream_t s) {
   const size_t smem_count = sizeof(int) * (2 * (size_t)p.E + p.R + (size_t)p.chunk_tokens * p.K);
   const size_t smem_assign = layout_assign_smem(p);
-  cudaError_t err;
-  if (smem_count > kDynSmemOptIn) {
-    err = cudaFuncSetAttribute(layout_count_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                               (int)smem_count);
-    if (err != cudaSuccess) return err;
-  }
-  if (smem_assign > kDynSmemOptIn) {
-    err = cudaFuncSetAttribute(layout_assign_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                               (int)smem_assign);
-    if (err != cudaSuccess) return err;
-  }
+  int dev = 0;
+  cudaError_t err = launch_geometry(reinterpret_cast<const void *>(layout_count_kernel), NTC,
+                                    smem_count, &dev, nullptr);
+  if (err != cudaSuccess) return err;
+  err = launch_geometry(reinterpret_cast<const void *>(layout_assign_kernel), NT, smem_assign,
+                        &dev, nullptr);
+  if (err != cudaSuccess) return err;
   layout_count_kernel<<<p.num_blocks, NTC, smem_count, s>>>(p);
   err = cudaGetLastError();
   if (err != cudaSuccess) return err;

@@ -135,6 +135,10 @@ __global__ void __launch_bounds__(kMaxConsumers + 32, 1)
     fence_mbar_init();
   }
   __syncthreads();
+  // Launched with programmatic dependent launch: the set-up above overlaps
+  // the tail of the kernel before this one; nothing below touches global
+  // memory before that kernel's writes are visible.
+  griddep_wait();
 
   if (warp == 0) {
     // ---------------- producer ----------------
@@ -303,8 +307,18 @@ cudaError_t launch_one(const CombineParams &p, int sm_cap, cudaStream_t s) {
   const int64_t units = (int64_t)p.T * nchunks;
   const int64_t grid = std::min<int64_t>((int64_t)use_sms * per_sm, units);
   if (grid <= 0) return cudaSuccess;
-  kern<<<(int)grid, threads, smem, s>>>(p, (int)chunk, nchunks, slots_cap);
-  return cudaGetLastError();
+  // programmatic dependent launch: the prologue overlaps the previous kernel
+  cudaLaunchConfig_t lc{};
+  lc.gridDim = dim3((unsigned)grid);
+  lc.blockDim = dim3(threads);
+  lc.dynamicSmemBytes = smem;
+  lc.stream = s;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  lc.attrs = attr;
+  lc.numAttrs = 1;
+  return cudaLaunchKernelEx(&lc, kern, p, (int)chunk, nchunks, slots_cap);
 }
 
 }  // namespace

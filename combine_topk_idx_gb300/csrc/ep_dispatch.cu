@@ -7,16 +7,18 @@
 //
 // Token-major scatter with persistent, warp-specialised CTAs:
 //   warp 0 (producer) takes tokens -- the CTA's index first, then the next
-//     free one from a handle counter -- reads each token's K destination rows
-//     (the next token's while the current one is issued), keeps the distinct ones
-//     (rank-layout slots of one rank share a row), writes the per-row weights
-//     and local expert ids, and issues one cp.async.bulk global->shared copy
-//     of the token's source row into a ring of input stages (3; 2 for
-//     quantised rows too large for three);
+//     free one from a handle counter -- issues one cp.async.bulk
+//     global->shared copy of the token's source row into a ring of input
+//     stages (3; 2 for quantised rows too large for three), then reads the
+//     token's K destination rows (fetched while the previous token was
+//     issued), keeps the distinct ones (rank-layout slots of one rank share a
+//     row) and writes the per-row weights and local expert ids;
 //   the consumer warps wait for a stage and
 //     FP8:  quantise it -- amax of each 128-element block by a 16-lane
-//           shuffle, scale = amax / 448 and x / scale with IEEE divisions,
-//           packed cvt.rn.satfinite.e4m3x2 -- into an output stage, then one
+//           shuffle, scale = amax / 448 (IEEE division) and the e4m3 bytes of
+//           x / scale (packed cvt.rn.satfinite.e4m3x2 of a bracket of the
+//           quotient, IEEE quotients wherever the bracket straddles a
+//           rounding boundary) -- into an output stage, then one
 //           thread issues one cp.async.bulk shared->global store per distinct
 //           destination row while the others write the scales;
 //     BF16: one thread stores the input stage itself to every row;
@@ -116,6 +118,42 @@ struct Routing {
   float w;
 };
 
+// e4m3 bytes of x / sc for eight elements (f: x as fp32), equal to the
+// round-to-nearest-even, saturating conversion of the IEEE fp32 quotients.
+// With r the reciprocal of sc within 2 ulp (relative error 2^-22), the
+// products x * r * (1 -+ 2^-17), each rounded, bracket the rounded quotient
+// strictly (every rounding error is below 2^-21 of the 2^-17 margin).  The
+// conversion is monotonic in the magnitude, so where both ends of the
+// bracket convert to the same byte, the quotient does too; where they differ
+// -- a rounding boundary of the e4m3 grid inside the bracket, about 1 element
+// in 200 of BF16 data, mostly exact ties -- the eight quotients are IEEE
+// divisions.  Outside sc in [2^-120, 2^120) the reciprocal loses its
+// accuracy and the divisions are always taken.
+__device__ __forceinline__ uint2 e4m3_block8(const float *f, float sc) {
+  const uint32_t sb = __float_as_uint(sc);
+  uint32_t c[4];
+  bool same = sb >= 0x03800000u && sb < 0x7B800000u;
+  if (same) {
+    const float r = __fdividef(1.0f, sc);
+    const float rl = r * 0.99999237060546875f, rh = r * 1.00000762939453125f;  // 1 -+ 2^-17
+    const uint64_t rl2 = f32x2_pack(rl, rl), rh2 = f32x2_pack(rh, rh);
+#pragma unroll
+    for (int q = 0; q < 4; ++q) {
+      const uint64_t x2 = f32x2_pack(f[2 * q], f[2 * q + 1]);
+      const uint64_t lo = f32x2_mul_rn(x2, rl2), hi = f32x2_mul_rn(x2, rh2);
+      const uint32_t cl = cvt_e4m3x2(f32x2_lo(lo), f32x2_hi(lo));
+      same &= cl == cvt_e4m3x2(f32x2_lo(hi), f32x2_hi(hi));
+      c[q] = cl;
+    }
+  }
+  if (!same) {
+#pragma unroll
+    for (int q = 0; q < 4; ++q)
+      c[q] = cvt_e4m3x2(__fdiv_rn(f[2 * q], sc), __fdiv_rn(f[2 * q + 1], sc));
+  }
+  return make_uint2(c[0] | (c[1] << 16), c[2] | (c[3] << 16));
+}
+
 __device__ __forceinline__ Routing load_routing(const DispatchParams &p, int t, int lane) {
   Routing r{-1, -1, 0.f};
   if (lane < p.K) {
@@ -158,6 +196,10 @@ __global__ void __launch_bounds__(kMaxConsumers + 32, 1) dispatch_kernel(Dispatc
     fence_mbar_init();
   }
   __syncthreads();
+  // Launched with programmatic dependent launch: the set-up above overlaps
+  // the tail of the kernel before this one; nothing below touches global
+  // memory before that kernel's writes are visible.
+  griddep_wait();
 
   // x rows and the destination payload are touched once: evict them first so
   // that the small, scattered scale-factor sectors stay in L2 until complete.
@@ -194,9 +236,17 @@ __global__ void __launch_bounds__(kMaxConsumers + 32, 1) dispatch_kernel(Dispatc
         }
         break;
       }
-      if (lane == 0) next = G + atomicAdd(p.sched, 1);
-      next = __shfl_sync(0xffffffffu, next, 0);
-      if (next < p.T) rn = load_routing(p, next, lane);
+      // The source row first: its load needs only the token index, so it
+      // overlaps the ticket for the next token and the routing work below.
+      // The stage completes once its bytes have landed and the producer has
+      // arrived after writing the row list.
+      if (lane == 0) {
+        mbar_expect_tx(&full[s], (uint32_t)in_bytes);
+        const void *src = MODE == kModePreq ? static_cast<const void *>(p.xq + (int64_t)t * H)
+                                            : static_cast<const void *>(p.x + (int64_t)t * H);
+        bulk_load_g2s_hint(in0 + s * in_stage, src, (uint32_t)in_bytes, &full[s], stream_pol);
+        next = G + atomicAdd(p.sched, 1);
+      }
       const unsigned peers = __match_any_sync(0xffffffffu, cur.d);
       const bool keep = cur.d >= 0 && lane == __ffs(peers) - 1;
       const unsigned keepm = __ballot_sync(0xffffffffu, keep);
@@ -209,30 +259,26 @@ __global__ void __launch_bounds__(kMaxConsumers + 32, 1) dispatch_kernel(Dispatc
       if (p.do_expand) {
         if (keep && p.recv_w != nullptr) p.recv_w[cur.d] = cur.w;
       } else if (p.recv_w != nullptr || p.recv_idx != nullptr) {
-        const int rk = keep ? cur.e / p.L : -1;
-        for (int kk = 0; kk < p.K; ++kk) {
-          const int ek = __shfl_sync(0xffffffffu, cur.e, kk);
-          const float wk = __shfl_sync(0xffffffffu, cur.w, kk);
-          if (keep) {
-            const bool same = ek >= 0 && ek / p.L == rk;
-            const int64_t o = (int64_t)cur.d * p.K + kk;
-            if (p.recv_w != nullptr) p.recv_w[o] = same ? wk : 0.f;
-            if (p.recv_idx != nullptr) p.recv_idx[o] = same ? ek - rk * p.L : -1;
+        // lane kk < K holds slot kk: its rank and local expert id once; then
+        // for each kept row, the K lanes write its K entries side by side
+        const int my_r = cur.e >= 0 ? cur.e / p.L : -1;
+        const int my_l = cur.e - my_r * p.L;
+        for (unsigned m = keepm; m; m &= m - 1) {
+          const int src = __ffs(m) - 1;
+          const int row = __shfl_sync(0xffffffffu, cur.d, src);
+          const int rr = __shfl_sync(0xffffffffu, my_r, src);
+          if (lane < p.K) {
+            const bool same = my_r >= 0 && my_r == rr;
+            const int64_t o = (int64_t)row * p.K + lane;
+            if (p.recv_w != nullptr) p.recv_w[o] = same ? cur.w : 0.f;
+            if (p.recv_idx != nullptr) p.recv_idx[o] = same ? my_l : -1;
           }
         }
       }
       __syncwarp();
-      if (lane == 0) {
-        if (n > 0) {
-          mbar_arrive_expect_tx(&full[s], (uint32_t)in_bytes);
-          const void *src = MODE == kModePreq
-                                ? static_cast<const void *>(p.xq + (int64_t)t * H)
-                                : static_cast<const void *>(p.x + (int64_t)t * H);
-          bulk_load_g2s_hint(in0 + s * in_stage, src, (uint32_t)in_bytes, &full[s], stream_pol);
-        } else {
-          mbar_arrive(&full[s]);
-        }
-      }
+      if (lane == 0) mbar_arrive(&full[s]);
+      next = __shfl_sync(0xffffffffu, next, 0);
+      if (next < p.T) rn = load_routing(p, next, lane);
     }
     return;
   }
@@ -294,11 +340,7 @@ __global__ void __launch_bounds__(kMaxConsumers + 32, 1) dispatch_kernel(Dispatc
             } else if (amax != 0.f) {
               // an infinite amax: finite elements divide to +-0, infinite ones
               // to NaN, which the conversion encodes as 0x7F
-              float g[8];
-#pragma unroll
-              for (int q = 0; q < 8; ++q) g[q] = __fdiv_rn(f[q], sc);
-              packed.x = cvt_e4m3x2(g[0], g[1]) | (cvt_e4m3x2(g[2], g[3]) << 16);
-              packed.y = cvt_e4m3x2(g[4], g[5]) | (cvt_e4m3x2(g[6], g[7]) << 16);
+              packed = e4m3_block8(f, sc);
             }
             *reinterpret_cast<uint2 *>(out + v * 8) = packed;
             if ((v & 15) == 0) {
@@ -460,7 +502,9 @@ __global__ void __launch_bounds__(256) sf_expand_kernel(DispatchParams p) {
   // Launched while the dispatch kernel still runs (programmatic dependent
   // launch).  With sf_wait the per-token scales come from that kernel: wait,
   // bounded, until every dispatch CTA has published its tokens' scales.
+  // The next kernel may start its own prologue at once.
   if (p.sf_wait == kSfWaitGrid) griddep_wait();
+  griddep_launch_dependents();
   __shared__ int ready;
   if (threadIdx.x == 0) {
     bool ok = true;
@@ -487,6 +531,9 @@ __global__ void __launch_bounds__(256) sf_expand_kernel(DispatchParams p) {
       }
     }
   }
+  // This kernel ends only after the dispatch kernel has: a kernel launched
+  // after it with programmatic dependent launch waits for this one alone.
+  if (p.sf_wait != kSfWaitGrid) griddep_wait();
 }
 
 template <int MODE, bool CM>
@@ -532,8 +579,20 @@ cudaError_t launch_one(const DispatchParams &p0, int sm_cap, cudaStream_t s) {
   p.sf_wait = MODE != kModeQuant ? kSfWaitNone
               : p.fixed_cap > 0  ? kSfWaitGrid
                                  : kSfWaitHandshake;
-  kern<<<(int)grid, threads, smem, s>>>(p);
-  err = cudaGetLastError();
+  {
+    // programmatic dependent launch: the prologue overlaps the previous kernel
+    cudaLaunchConfig_t lc{};
+    lc.gridDim = dim3((unsigned)grid);
+    lc.blockDim = dim3(threads);
+    lc.dynamicSmemBytes = smem;
+    lc.stream = s;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    lc.attrs = attr;
+    lc.numAttrs = 1;
+    err = cudaLaunchKernelEx(&lc, kern, p);
+  }
   if (err != cudaSuccess || MODE == kModeBf16 || !CM) return err;
   // column-major scales: one gather pass (rows past the real total, in an
   // upper-bound allocation, are left untouched; so are the unused rows of a

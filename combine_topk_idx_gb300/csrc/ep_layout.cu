@@ -216,6 +216,7 @@ __global__ void __launch_bounds__(NT, 1) layout_assign_kernel(LayoutParams p) {
   for (int i = threadIdx.x; i < nrw * nkey; i += NT) whist[i] = 0ull;
   for (int e = threadIdx.x; e < E; e += NT) rank_of[e] = e / L;
   griddep_wait();  // everything below reads the count kernel's outputs
+  griddep_launch_dependents();  // the next kernel (dispatch) may start its prologue
   for (int i = threadIdx.x; i < ns; i += NT) idx_s[i] = p.topk32[base + i];
   // Column sums of the per-chunk histograms: global totals and this chunk's
   // offset.  g consecutive lanes share a key and split its chunks.

@@ -469,16 +469,44 @@ class GpuWorkload:
 
     def step(self, ev=None):
         """One back-to-back step: layout -> dispatch -> combine, nothing
-        between them on the device.  ev (5 events): layout start / end,
-        dispatch start, dispatch end = combine start, combine end.  Without
-        the count wait every launch is enqueued behind a spin kernel, so no
-        host code runs inside a timed interval; with it the host waits for
-        the counts (the layout interval includes that reaction, as it does
-        for every caller of the exact allocation) and the dispatch and
-        combine launches are enqueued behind the spin kernel."""
+        between them on the device, every launch enqueued behind a spin
+        kernel so no host code runs inside a timed interval.  ev (4 events):
+        without the count wait one interval [ev0, ev3] covers the step, with
+        no event between the kernels (so each may start while the one before
+        it drains, as the kernels are launched); with it the layout interval
+        [ev0, ev1] includes the host's reaction to the counts (as for every
+        caller of the exact allocation), and [ev2, ev3] covers dispatch and
+        combine, enqueued behind a second spin kernel."""
         ep, sync = self.ep, bool(self.cfg.do_cpu_sync)
-        if not sync:
+        self._gate()
+        if ev:
+            ev[0].record(self.stream)
+        h = ep.ep_layout(self.cfg, self.idx)
+        if ev and sync:
+            ev[1].record(self.stream)
+        out = ep.alloc_recv(h, with_weights=True, with_idx=True)
+        if sync:
             self._gate()
+            if ev:
+                ev[2].record(self.stream)
+        ep.ep_dispatch(h, self.x, self.w, **out)
+        ep.ep_combine(h, self.y, self.w, None, None, self.eb, out=self.out_comb)
+        if ev:
+            ev[3].record(self.stream)
+        h.free()
+
+    def step_time(self, ev) -> float:
+        if self.cfg.do_cpu_sync:
+            return ev[0].elapsed_time(ev[1]) + ev[2].elapsed_time(ev[3])
+        return ev[0].elapsed_time(ev[3])
+
+    def step_staged(self, ev=None):
+        """The back-to-back step with an event between consecutive stages, for
+        the per-stage breakdown (the events keep each kernel from starting
+        before the one before it has ended).  ev (5 events): layout start /
+        end, dispatch start, dispatch end = combine start, combine end."""
+        ep, sync = self.ep, bool(self.cfg.do_cpu_sync)
+        self._gate()
         if ev:
             ev[0].record(self.stream)
         h = ep.ep_layout(self.cfg, self.idx)
@@ -523,10 +551,24 @@ class GpuWorkload:
             ev[5].record(self.stream)
         h.free()
 
+    def run_whole_steps(self, n: int, warmup: int) -> float:
+        """Warm-up, then n back-to-back steps with the L2 flushed between
+        steps; returns the mean step time (ms)."""
+        for _ in range(warmup):
+            self.flush_l2()
+            self.step()
+        torch.cuda.synchronize()
+        evs = [[torch.cuda.Event(enable_timing=True) for _ in range(4)] for _ in range(n)]
+        for i in range(n):
+            self.flush_l2()
+            self.step(evs[i])
+        torch.cuda.synchronize()
+        return statistics.mean(self.step_time(e) for e in evs)
+
     def run_steps(self, n: int, warmup: int, flushed: bool = False) -> dict:
-        """Warm-up, then n steps with the L2 flushed between steps; returns the
-        mean per-stage device times (ms)."""
-        fn = self.step_flushed if flushed else self.step
+        """Warm-up, then n staged steps with the L2 flushed between steps;
+        returns the mean per-stage device times (ms)."""
+        fn = self.step_flushed if flushed else self.step_staged
         for _ in range(warmup):
             if not flushed:
                 self.flush_l2()
@@ -643,25 +685,23 @@ def run_gpu(args, ws, rank, local):
         flush_l2()
         main.step()
     torch.cuda.synchronize()
-    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(5)] for _ in range(args.steps)]
+    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(4)] for _ in range(args.steps)]
     barrier(ws)
     with clocks.section("timed_steps"):
         for i in range(args.steps):
             flush_l2()
             main.step(evs[i])
     barrier(ws)
-    lay_ms = [e[0].elapsed_time(e[1]) for e in evs]
-    dis_ms = [e[2].elapsed_time(e[3]) for e in evs]
-    com_ms = [e[3].elapsed_time(e[4]) for e in evs]
-    step_ms = statistics.mean(a + b + c for a, b, c in zip(lay_ms, dis_ms, com_ms))
+    step_ms = statistics.mean(main.step_time(e) for e in evs)
     step_ms_max = max_over_ranks(step_ms, ws, dev)
     value = total_bytes * ws / (step_ms_max * 1e-3) / 1e9
     n_launch = args.steps * sum(main.n_launch.values())
-    t_main = {"layout": statistics.mean(lay_ms), "dispatch": statistics.mean(dis_ms),
-              "combine": statistics.mean(com_ms), "step": step_ms}
 
     # ---- secondary figures on the same workload ----
+    # per-stage breakdown of the same step (an event between stages)
     fl_steps = max(8, args.steps // 2)
+    with clocks.section("stages_staged"):
+        t_main = main.run_steps(fl_steps, 3)
     with clocks.section("stages_flushed"):
         t_fl = main.run_steps(fl_steps, 3, flushed=True)
     with clocks.section("sustained"):
@@ -817,9 +857,11 @@ def run_gpu(args, ws, rank, local):
                      if n != wl.name]:
             other = GpuWorkload(ep, W.WORKLOADS[name], dev, args.seed, stream, flush_l2)
             with clocks.section(f"workload_{name}"):
+                tw = other.run_whole_steps(args.workload_steps, 3)
                 tb = other.run_steps(args.workload_steps, 3)
                 tf = other.run_steps(args.workload_steps, 3, flushed=True)
                 su = other.sustained(args.workload_steps, peak)
+            whole = sum(other.by.values())
             wl_block[name] = {
                 "config": {"tokens": other.T, "hidden": other.H,
                            "experts": other.wl.num_experts,
@@ -828,6 +870,10 @@ def run_gpu(args, ws, rank, local):
                            "do_cpu_sync": other.wl.do_cpu_sync,
                            "fixed_capacity": other.wl.fixed_capacity},
                 "steps": args.workload_steps,
+                "step": {"ms": round(tw, 5), "bytes": whole,
+                         "gbs": round(whole / tw / 1e6, 1),
+                         "frac_of_peak": round(whole / tw / 1e6 / peak, 4),
+                         "tokens_per_s": round(other.T / (tw * 1e-3), 1)},
                 "back_to_back": other.stage_block(tb, peak),
                 "stages_flushed": other.stage_block(tf, peak),
                 "sustained": su,
@@ -858,11 +904,16 @@ def run_gpu(args, ws, rank, local):
                    "parallelism": f"replicas x{ws}"},
         "tokens_per_s": round(T * ws / (step_ms_max * 1e-3), 1),
         "pct_of_hbm_peak": round(100 * value / ws / peak, 2),
-        "stages": {k: v for k, v in stages.items() if k != "step"},
-        "stages_how": "one step = layout, dispatch, combine back to back on the device; the "
-                      "dispatch and combine launches are enqueued behind a spin kernel after "
-                      "the count wait, so no host code falls inside their intervals; the "
-                      "layout interval includes the host's reaction to the count wait",
+        "step_how": "one step = layout, dispatch, combine back to back on the device, "
+                    "launches enqueued behind a spin kernel so no host code falls inside the "
+                    "timed intervals: the layout interval (it includes the host's reaction to "
+                    "the count wait) plus one interval over dispatch and combine, with no "
+                    "event between the kernels",
+        "stages": {**{k: v for k, v in stages.items() if k != "step"},
+                   "staged_step_ms": round(t_main["step"], 5), "steps": fl_steps},
+        "stages_how": "the same step with an event between consecutive stages (each kernel "
+                      "then starts only after the one before it has ended): per-stage device "
+                      "times",
         "layout_plus_dispatch_ms": round(t_main["layout"] + d_ms, 5),
         "layout_host_ms": round(1e3 * statistics.median(layout_host_s), 5),
         "stages_flushed": {**{k: v for k, v in main.stage_block(t_fl, peak).items()},

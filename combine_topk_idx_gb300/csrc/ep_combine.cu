@@ -15,11 +15,11 @@
 //     counted on the stage's "full" mbarrier;
 //   the other warps (consumers) wait for a stage and accumulate its rows
 //     strictly in slot order -- per-expert bias added to each row first (a
-//     small table reused by every token: read through L1, not staged), then
+//     small table reused by every token: read through L1, not staged; one
+//     mixed-precision BF16 + fp32 add per element), then
 //     separately rounded fp32 multiplies and adds (__fmul_rn / __fadd_rn:
-//     never contracted to an FMA; the compiler may fuse a packed f32x2
-//     multiply into a following packed add, so packed adds serve only the
-//     bias sum) -- add the per-token biases, round to BF16 (nearest even),
+//     never contracted to an FMA) -- add the per-token biases, round to
+//     BF16 (nearest even),
 //     store the output chunk and release the stage on its "empty" mbarrier.
 // Each output element is written by exactly one thread: no atomics.  Every
 // mbarrier wait is bounded; a wait that gives up sets EP_ERRBIT_TIMEOUT in
@@ -50,19 +50,6 @@ __device__ __forceinline__ void unpack8(const uint4 &v, float *f) {
   f[2] = bf16_lo(v.y); f[3] = bf16_hi(v.y);
   f[4] = bf16_lo(v.z); f[5] = bf16_hi(v.z);
   f[6] = bf16_lo(v.w); f[7] = bf16_hi(v.w);
-}
-
-// Eight BF16 pairs summed in fp32, element by element (each sum rounded to
-// nearest even), with packed f32x2 adds.
-__device__ __forceinline__ void add8_bf16(const uint4 &a, const uint4 &b, float *f) {
-  const uint64_t s0 = f32x2_add_rn(bf16x2_to_f32x2(a.x), bf16x2_to_f32x2(b.x));
-  const uint64_t s1 = f32x2_add_rn(bf16x2_to_f32x2(a.y), bf16x2_to_f32x2(b.y));
-  const uint64_t s2 = f32x2_add_rn(bf16x2_to_f32x2(a.z), bf16x2_to_f32x2(b.z));
-  const uint64_t s3 = f32x2_add_rn(bf16x2_to_f32x2(a.w), bf16x2_to_f32x2(b.w));
-  f[0] = f32x2_lo(s0); f[1] = f32x2_hi(s0);
-  f[2] = f32x2_lo(s1); f[3] = f32x2_hi(s1);
-  f[4] = f32x2_lo(s2); f[5] = f32x2_hi(s2);
-  f[6] = f32x2_lo(s3); f[7] = f32x2_hi(s3);
 }
 
 struct Routing {
@@ -237,13 +224,18 @@ __global__ void __launch_bounds__(kMaxConsumers + 32, 1)
       float acc[8];
 #pragma unroll
       for (int q = 0; q < 8; ++q) acc[q] = 0.f;
+      const uint16_t *eb_v = HAS_EB ? p.ebias + off / 2 + v * 8 : nullptr;  // this vector's bias
       for (int j = 0; j < n; ++j) {
         float f[8];
         if (HAS_EB) {
-          // y + expert bias, two lanes per packed add (no multiply feeds it,
-          // so nothing can be contracted)
-          const uint4 bv = ld_cached_v4(p.ebias + (int64_t)meta[s].e[j] * H + off / 2 + v * 8);
-          add8_bf16(*reinterpret_cast<const uint4 *>(sb + (int64_t)j * chunk_bytes + v * 16), bv, f);
+          // y + expert bias: one mixed-precision add per element, y taken as
+          // BF16 straight from its half-word, the bias widened to fp32
+          const uint4 bv = ld_cached_v4(eb_v + (int64_t)meta[s].e[j] * H);
+          const uint4 yv = *reinterpret_cast<const uint4 *>(sb + (int64_t)j * chunk_bytes + v * 16);
+          add2_bf16_f32(yv.x, bf16_lo(bv.x), bf16_hi(bv.x), f[0], f[1]);
+          add2_bf16_f32(yv.y, bf16_lo(bv.y), bf16_hi(bv.y), f[2], f[3]);
+          add2_bf16_f32(yv.z, bf16_lo(bv.z), bf16_hi(bv.z), f[4], f[5]);
+          add2_bf16_f32(yv.w, bf16_lo(bv.w), bf16_hi(bv.w), f[6], f[7]);
         } else {
           unpack8(*reinterpret_cast<const uint4 *>(sb + (int64_t)j * chunk_bytes + v * 16), f);
         }

@@ -82,9 +82,9 @@ __device__ __forceinline__ float bf16_lo(uint32_t w) { return __uint_as_float(w 
 __device__ __forceinline__ float bf16_hi(uint32_t w) { return __uint_as_float(w & 0xffff0000u); }
 
 // Two fp32 lanes in one 64-bit register (lane 0 in the low word), for the
-// packed f32x2 arithmetic of sm_100 and later: each lane is rounded to
-// nearest even exactly like the scalar add.rn.f32 / mul.rn.f32, and no
-// multiply-add is ever contracted.
+// packed f32x2 multiplies of sm_100 and later (each lane rounded to nearest
+// even like mul.rn.f32).  They only feed conversions here: a packed multiply
+// followed by a packed add may be contracted into a fused multiply-add.
 __device__ __forceinline__ uint64_t f32x2_pack(float lo, float hi) {
   uint64_t r;
   asm("mov.b64 %0, {%1, %2};" : "=l"(r) : "f"(lo), "f"(hi));
@@ -100,19 +100,20 @@ __device__ __forceinline__ float f32x2_hi(uint64_t v) {
   asm("mov.b64 {%0, %1}, %2;" : "=f"(lo), "=f"(hi) : "l"(v));
   return hi;
 }
-__device__ __forceinline__ uint64_t f32x2_add_rn(uint64_t a, uint64_t b) {
-  uint64_t d;
-  asm("add.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
-  return d;
-}
 __device__ __forceinline__ uint64_t f32x2_mul_rn(uint64_t a, uint64_t b) {
   uint64_t d;
   asm("mul.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
   return d;
 }
-// A BF16 pair (element 0 in the low half) -> two fp32 lanes (exact).
-__device__ __forceinline__ uint64_t bf16x2_to_f32x2(uint32_t w) {
-  return f32x2_pack(bf16_lo(w), bf16_hi(w));
+// The BF16 halves of w (low half first) plus fp32 addends a0, a1: two
+// mixed-precision add.rn.f32.bf16, i.e. the BF16 value widened exactly and the
+// sum rounded once to fp32 -- the same as __fadd_rn(float(h), a).
+__device__ __forceinline__ void add2_bf16_f32(uint32_t w, float a0, float a1, float &d0,
+                                              float &d1) {
+  asm("{\n\t.reg .b16 l, h;\n\tmov.b32 {l, h}, %2;\n\t"
+      "add.rn.f32.bf16 %0, l, %3;\n\tadd.rn.f32.bf16 %1, h, %4;\n\t}"
+      : "=f"(d0), "=f"(d1)
+      : "r"(w), "f"(a0), "f"(a1));
 }
 
 // Maximum that returns NaN when either operand is NaN (fmaxf drops it).

@@ -126,14 +126,14 @@ struct Routing {
 // conversion is monotonic in the magnitude, so where both ends of the
 // bracket convert to the same byte, the quotient does too; where they differ
 // -- a rounding boundary of the e4m3 grid inside the bracket, about 1 element
-// in 200 of BF16 data, mostly exact ties -- the eight quotients are IEEE
-// divisions.  Outside sc in [2^-120, 2^120) the reciprocal loses its
-// accuracy and the divisions are always taken.
+// in 200 of BF16 data, mostly exact ties -- that pair of quotients is taken
+// by IEEE division (per pair, so a warp runs the divisions only for pairs
+// where some lane needs them).  Outside sc in [2^-120, 2^120) the reciprocal
+// loses its accuracy and every quotient is a division.
 __device__ __forceinline__ uint2 e4m3_block8(const float *f, float sc) {
   const uint32_t sb = __float_as_uint(sc);
   uint32_t c[4];
-  bool same = sb >= 0x03800000u && sb < 0x7B800000u;
-  if (same) {
+  if (sb >= 0x03800000u && sb < 0x7B800000u) {
     const float r = __fdividef(1.0f, sc);
     const float rl = r * 0.99999237060546875f, rh = r * 1.00000762939453125f;  // 1 -+ 2^-17
     const uint64_t rl2 = f32x2_pack(rl, rl), rh2 = f32x2_pack(rh, rh);
@@ -141,12 +141,11 @@ __device__ __forceinline__ uint2 e4m3_block8(const float *f, float sc) {
     for (int q = 0; q < 4; ++q) {
       const uint64_t x2 = f32x2_pack(f[2 * q], f[2 * q + 1]);
       const uint64_t lo = f32x2_mul_rn(x2, rl2), hi = f32x2_mul_rn(x2, rh2);
-      const uint32_t cl = cvt_e4m3x2(f32x2_lo(lo), f32x2_hi(lo));
-      same &= cl == cvt_e4m3x2(f32x2_lo(hi), f32x2_hi(hi));
-      c[q] = cl;
+      c[q] = cvt_e4m3x2(f32x2_lo(lo), f32x2_hi(lo));
+      if (c[q] != cvt_e4m3x2(f32x2_lo(hi), f32x2_hi(hi)))
+        c[q] = cvt_e4m3x2(__fdiv_rn(f[2 * q], sc), __fdiv_rn(f[2 * q + 1], sc));
     }
-  }
-  if (!same) {
+  } else {
 #pragma unroll
     for (int q = 0; q < 4; ++q)
       c[q] = cvt_e4m3x2(__fdiv_rn(f[2 * q], sc), __fdiv_rn(f[2 * q + 1], sc));
@@ -291,6 +290,11 @@ __global__ void __launch_bounds__(kMaxConsumers + 32, 1) dispatch_kernel(Dispatc
   const int npad = pad_work ? __ldg(p.psum_pad + p.E) : 0;
   const int64_t pad_items = (npad + kPadRowsPerItem - 1) / kPadRowsPerItem;
   uint8_t *recv = static_cast<uint8_t *>(p.recv_x);
+  // row-major scale stores: when nb divides the consumer count, thread ctid
+  // owns scale column ctid % nb of rows ctid / nb, + nct / nb, ...
+  const int sf_step = (nb > 0 && nct % nb == 0) ? nct / nb : 0;
+  const int sf_j = sf_step > 0 ? ctid % nb : 0;
+  const int sf_r0 = sf_step > 0 ? ctid / nb : 0;
   for (int64_t i = 0;; ++i) {
     const int s = (int)(i % S);
     const uint32_t par = (uint32_t)((i / S) & 1);
@@ -360,9 +364,14 @@ __global__ void __launch_bounds__(kMaxConsumers + 32, 1) dispatch_kernel(Dispatc
           bulk_commit();
         }
         if (!COL_MAJOR) {  // row-major scales: nb contiguous floats per row
-          for (int e = ctid; e < n * nb; e += nct) {
-            const int r = e / nb, j = e - r * nb;
-            p.recv_sf[(int64_t)meta[s].rows[r] * nb + j] = sf[j];
+          if (sf_step > 0) {  // every thread keeps its column sf_j, rows sf_r0, +sf_step, ...
+            for (int r = sf_r0; r < n; r += sf_step)
+              p.recv_sf[(int64_t)meta[s].rows[r] * nb + sf_j] = sf[sf_j];
+          } else {
+            for (int e = ctid; e < n * nb; e += nct) {
+              const int r = e / nb, j = e - r * nb;
+              p.recv_sf[(int64_t)meta[s].rows[r] * nb + j] = sf[j];
+            }
           }
         }
       } else if (ctid == 0) {

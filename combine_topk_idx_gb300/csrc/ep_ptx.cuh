@@ -90,15 +90,9 @@ __device__ __forceinline__ uint64_t f32x2_pack(float lo, float hi) {
   asm("mov.b64 %0, {%1, %2};" : "=l"(r) : "f"(lo), "f"(hi));
   return r;
 }
-__device__ __forceinline__ float f32x2_lo(uint64_t v) {
-  float lo, hi;
-  asm("mov.b64 {%0, %1}, %2;" : "=f"(lo), "=f"(hi) : "l"(v));
-  return lo;
-}
+__device__ __forceinline__ float f32x2_lo(uint64_t v) { return __uint_as_float((uint32_t)v); }
 __device__ __forceinline__ float f32x2_hi(uint64_t v) {
-  float lo, hi;
-  asm("mov.b64 {%0, %1}, %2;" : "=f"(lo), "=f"(hi) : "l"(v));
-  return hi;
+  return __uint_as_float((uint32_t)(v >> 32));
 }
 __device__ __forceinline__ uint64_t f32x2_mul_rn(uint64_t a, uint64_t b) {
   uint64_t d;

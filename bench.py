@@ -614,6 +614,42 @@ class GpuWorkload:
         n = max(1, min(4, -(-2 * L2_BYTES // max(1, t.numel() * t.element_size()))))
         return [t] + [t.clone() for _ in range(n - 1)]
 
+    def soak(self, seconds: float, peak: float) -> dict:
+        """Dispatch + combine pairs launched back to back for about `seconds`
+        (inputs rotating over copies larger than L2); throughput over the
+        whole run, which reaches the power and thermal steady state."""
+        ep = self.ep
+        h = ep.ep_layout(self.cfg, self.idx)
+        out = ep.alloc_recv(h, with_weights=True, with_idx=True)
+        xs, ys = self._copies(self.x), self._copies(self.y)
+
+        def pair(i):
+            ep.ep_dispatch(h, xs[i % len(xs)], self.w, **out)
+            ep.ep_combine(h, ys[i % len(ys)], self.w, None, None, self.eb, out=self.out_comb)
+
+        for i in range(3):
+            pair(i)
+        torch.cuda.synchronize()
+        t0 = time.perf_counter()
+        pair(0)
+        torch.cuda.synchronize()
+        one = max(time.perf_counter() - t0, 1e-5)
+        n = max(10, int(seconds / one))
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        self._gate()
+        e0.record(self.stream)
+        for i in range(n):
+            pair(i)
+        e1.record(self.stream)
+        torch.cuda.synchronize()
+        ms = e0.elapsed_time(e1)
+        by = self.by["dispatch"] + self.by["combine"]
+        gbs = by * n / (ms * 1e-3) / 1e9
+        h.free()
+        return {"pairs": n, "seconds": round(ms * 1e-3, 3), "gbs": round(gbs, 1),
+                "frac_of_peak": round(gbs / peak, 4), "gpu_launches": n * (
+                    self.n_launch["dispatch"] + self.n_launch["combine"])}
+
     def sustained(self, n: int, peak: float) -> dict:
         """Dispatch alone, then combine alone, launched n times back to back
         behind a spin kernel: each launch pays the write-back of the lines the
@@ -706,6 +742,12 @@ def run_gpu(args, ws, rank, local):
         t_fl = main.run_steps(fl_steps, 3, flushed=True)
     with clocks.section("sustained"):
         sus = main.sustained(max(10, args.steps // 2), peak)
+    # Soak: dispatch and combine back to back for about args.soak_s seconds
+    # (power and thermal steady state); most clock samples come from here.
+    soak = None
+    if args.soak_s > 0:
+        with clocks.section("soak"):
+            soak = main.soak(args.soak_s, peak)
     # Host wall time of the layout call on an idle GPU (with do_cpu_sync it
     # includes the count wait).
     layout_host_s = []
@@ -924,6 +966,7 @@ def run_gpu(args, ws, rank, local):
                                     "inputs rotating over copies larger than L2: every launch "
                                     "pays the write-back of its predecessor's dirty lines, in "
                                     "steady state its own"},
+        "soak": soak,
         "roofline": {"bound": "hbm", "kernel": dom, "achieved": round(achieved, 1),
                      "peak": peak, "peak_source": peaks["source"], "unit": "GB/s",
                      "frac": round(achieved / peak, 4), "traffic": traffic,
@@ -970,6 +1013,61 @@ def run_gpu(args, ws, rank, local):
         torch.distributed.destroy_process_group()
     if rank == 0:
         print(json.dumps(line), flush=True)
+
+
+def run_stage(args):
+    """One stage of one workload launched --stage-launches times through the C
+    ABI, L2 flushed (256 MiB write + 256 MiB read) before each launch; prints
+    the mean device time.  Meant for profiling a single kernel (ncu -k ... -s
+    ... -c ...); the step benchmark above is the measurement."""
+    import combine_topk_idx_gb300 as ep
+    dev = torch.device("cuda", 0)
+    torch.cuda.set_device(dev)
+    ep.load_library()
+    wl = W.WORKLOADS[args.workload]
+    inp = W.make_inputs(wl, seed=args.seed)
+    idx, w, x = inp["topk_idx"].to(dev), inp["topk_weights"].to(dev), inp["x"].to(dev)
+    eb = inp["expert_bias"].to(dev) if inp["expert_bias"] is not None else None
+    cfg = ep.make_config(wl.num_tokens, wl.num_topk, wl.num_experts, wl.num_ranks, wl.hidden,
+                         wl.num_max_tokens_per_rank, wl.expert_alignment, wl.do_expand,
+                         wl.do_zero_padding, wl.do_cpu_sync, wl.use_fp8, wl.col_major_sf,
+                         fixed_capacity=wl.fixed_capacity)
+    h = ep.ep_layout(cfg, idx)
+    out = ep.alloc_recv(h, with_weights=True, with_idx=True)
+    y = W.make_bf16_rows(h.rows_alloc, wl.hidden, args.seed).to(dev)
+    res = torch.empty((wl.num_tokens, wl.hidden), dtype=torch.bfloat16, device=dev)
+    g_recv = torch.empty((h.rows_alloc, wl.hidden), dtype=torch.bfloat16, device=dev)
+    g_w = torch.empty((wl.num_tokens, wl.num_topk), dtype=torch.float32, device=dev)
+    grad_recv_w = torch.zeros(out["recv_topk_weights"].shape, dtype=torch.float32, device=dev)
+    flush_w = torch.empty(L2_FLUSH_BYTES // 4, dtype=torch.float32, device=dev)
+    flush_r = torch.ones(L2_FLUSH_BYTES // 4, dtype=torch.float32, device=dev)
+
+    def launch():
+        if args.stage == "layout":
+            ep.ep_layout(cfg, idx).free()
+        elif args.stage == "dispatch":
+            ep.ep_dispatch(h, x, w, **out)
+        elif args.stage == "combine":
+            ep.ep_combine(h, y, w, None, None, eb, out=res)
+        elif args.stage == "combine_backward":
+            ep.ep_combine_backward(h, x, g_recv)
+        else:  # dispatch_backward
+            ep.ep_dispatch_backward(h, y, grad_recv_w, res, g_w)
+
+    ms = []
+    for _ in range(args.stage_launches):
+        flush_w.zero_()
+        flush_r.sum()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record()
+        launch()
+        e1.record()
+        torch.cuda.synchronize()
+        ms.append(e0.elapsed_time(e1))
+    h.free()
+    print(json.dumps({"stage": args.stage, "workload": wl.name, "launches": len(ms),
+                      "ms_mean": round(statistics.mean(ms), 5),
+                      "l2": "flushed before each launch"}), flush=True)
 
 
 def run_reference(args, ws, rank):
@@ -1029,10 +1127,19 @@ def main(argv=None):
     ap.add_argument("--no-workloads", action="store_true",
                     help="skip the block that times every other workload")
     ap.add_argument("--workload-steps", type=int, default=10)
+    ap.add_argument("--stage", choices=["layout", "dispatch", "combine", "combine_backward",
+                                        "dispatch_backward"],
+                    help="launch one stage only (for profiling one kernel)")
+    ap.add_argument("--stage-launches", type=int, default=4)
+    ap.add_argument("--soak-s", type=float, default=1.5,
+                    help="seconds of back-to-back dispatch + combine at the end (0: none)")
     args = ap.parse_args(argv)
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")
     ws, rank, local = dist_env()
+    if args.stage:
+        run_stage(args)
+        return
     if args.impl == "reference":
         run_reference(args, ws, rank)
         return

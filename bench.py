@@ -400,10 +400,11 @@ def bytes_from_layout(wl, T, topk_idx, lay: dict) -> dict:
 GATE_CYCLES = 2_000_000   # ~1 ms spin: the host enqueues the timed launches behind it
 L2_BYTES = 126 << 20      # GB300 L2; inputs re-read by repeated launches rotate past it
 
-# Kernels each stage launches (ours): layout = count + assign; dispatch = copy
-# kernel (+ the column-major scale gather for FP8); combine = one kernel.
-def launches(wl: W.Workload, rows_alloc: int, T: int) -> dict:
-    return {"layout": 2,
+# Kernels each stage launches (ours): layout = one cluster kernel or count +
+# assign (the library reports which); dispatch = copy kernel (+ the
+# column-major scale gather for FP8); combine = one kernel.
+def launches(wl: W.Workload, rows_alloc: int, T: int, layout_kernels: int) -> dict:
+    return {"layout": layout_kernels,
             "dispatch": (1 + int(wl.use_fp8 and wl.col_major_sf)) if rows_alloc > 0 else 0,
             "combine": 1 if T > 0 else 0}
 
@@ -460,7 +461,7 @@ class GpuWorkload:
         self.out_comb = torch.empty((T, H), dtype=torch.bfloat16, device=dev)
         self.grad_recv_w = out0["recv_topk_weights"].clone()
         self.rows_alloc = rows
-        self.n_launch = launches(wl, rows, T)
+        self.n_launch = launches(wl, rows, T, int(h0.info.layout_kernels))
         h0.free()
         del out0
 
@@ -473,23 +474,29 @@ class GpuWorkload:
         kernel so no host code runs inside a timed interval.  ev (4 events):
         without the count wait one interval [ev0, ev3] covers the step, with
         no event between the kernels (so each may start while the one before
-        it drains, as the kernels are launched); with it the layout interval
-        [ev0, ev1] includes the host's reaction to the counts (as for every
-        caller of the exact allocation), and [ev2, ev3] covers dispatch and
-        combine, enqueued behind a second spin kernel."""
+        it drains, as the kernels are launched), layout and dispatch by one
+        ep_layout_dispatch call into buffers sized from the configuration;
+        with it the layout interval [ev0, ev1] includes the host's reaction
+        to the counts (as for every caller of the exact allocation), and
+        [ev2, ev3] covers dispatch and combine, enqueued behind a second spin
+        kernel."""
         ep, sync = self.ep, bool(self.cfg.do_cpu_sync)
+        if not sync:  # host-side allocation (torch's caching allocator), before the gate
+            out = ep.alloc_recv_planned(self.cfg, with_weights=True, with_idx=True)
         self._gate()
         if ev:
             ev[0].record(self.stream)
-        h = ep.ep_layout(self.cfg, self.idx)
-        if ev and sync:
-            ev[1].record(self.stream)
-        out = ep.alloc_recv(h, with_weights=True, with_idx=True)
         if sync:
+            h = ep.ep_layout(self.cfg, self.idx)
+            if ev:
+                ev[1].record(self.stream)
+            out = ep.alloc_recv(h, with_weights=True, with_idx=True)
             self._gate()
             if ev:
                 ev[2].record(self.stream)
-        ep.ep_dispatch(h, self.x, self.w, **out)
+            ep.ep_dispatch(h, self.x, self.w, **out)
+        else:
+            h = ep.ep_layout_dispatch(self.cfg, self.idx, self.x, self.w, **out)
         ep.ep_combine(h, self.y, self.w, None, None, self.eb, out=self.out_comb)
         if ev:
             ev[3].record(self.stream)
@@ -915,7 +922,10 @@ def run_gpu(args, ws, rank, local):
                 "step": {"ms": round(tw, 5), "bytes": whole,
                          "gbs": round(whole / tw / 1e6, 1),
                          "frac_of_peak": round(whole / tw / 1e6 / peak, 4),
-                         "tokens_per_s": round(other.T / (tw * 1e-3), 1)},
+                         "tokens_per_s": round(other.T / (tw * 1e-3), 1),
+                         "calls": ("ep_layout (count wait), ep_dispatch, ep_combine"
+                                   if other.wl.do_cpu_sync else
+                                   "ep_layout_dispatch, ep_combine")},
                 "back_to_back": other.stage_block(tb, peak),
                 "stages_flushed": other.stage_block(tf, peak),
                 "sustained": su,

@@ -13,5 +13,5 @@ from ._binding import (  # noqa: F401
     load_library, make_config, status_string, upper_bound_rows, validate_config,
     EP_NOALLOC_SCRATCH_WORDS, EpLayoutBuffersC, alloc_layout_buffers, ep_layout_noalloc,
     EP_ERRBIT_TIMEOUT, selftest_bounded_wait, ep_combine_backward, ep_dispatch_backward,
-    ep_dispatch_fp8,
+    ep_dispatch_fp8, alloc_recv_planned, ep_layout_dispatch, plan_layout,
 )

@@ -86,6 +86,8 @@ class EpLayoutInfoC(ctypes.Structure):
         ("meta_rows", ctypes.c_int64),
         ("expert_capacity", ctypes.c_int64),
         ("sf_expert_stride", ctypes.c_int64),
+        ("layout_kernels", ctypes.c_int32),
+        ("reserved1", ctypes.c_int32),
     ]
 
 
@@ -127,6 +129,11 @@ def load_library(path: str = LIB_PATH) -> ctypes.CDLL:
     lib.ep_upper_bound_rows.restype = ctypes.c_int
     lib.ep_host_wait_flag.argtypes = [ctypes.POINTER(i32), i32, i32]
     lib.ep_host_wait_flag.restype = ctypes.c_int
+    lib.ep_plan_layout.argtypes = [ctypes.POINTER(EpConfigC), ctypes.POINTER(EpLayoutInfoC)]
+    lib.ep_plan_layout.restype = ctypes.c_int
+    lib.ep_layout_dispatch.argtypes = [ctypes.POINTER(EpConfigC), vp, vp, vp, vp, vp, vp, vp, vp,
+                                       ctypes.POINTER(vp), ctypes.POINTER(EpLayoutInfoC)]
+    lib.ep_layout_dispatch.restype = ctypes.c_int
     if lib.ep_abi_version() != EP_ABI_VERSION:
         raise RuntimeError("libep.so ABI version does not match this binding")
     _lib = lib
@@ -286,28 +293,78 @@ def ep_layout(cfg: EpConfigC, topk_idx: torch.Tensor, stream=None) -> Handle:
     return Handle(h.value, cfg_copy, info, st)
 
 
-def alloc_recv(handle: Handle, with_weights: bool = False, with_idx: bool = False,
-               zero: bool = False) -> dict:
-    """Allocate the dispatch outputs for ``handle`` with torch (device memory only)."""
-    rows, H, K = handle.rows_alloc, handle.H, handle.K
+def _alloc(cfg: EpConfigC, info: EpLayoutInfoC, with_weights: bool, with_idx: bool,
+           zero: bool) -> dict:
+    rows, H, K = int(info.rows_alloc), cfg.hidden, cfg.num_topk
     mk = torch.zeros if zero else torch.empty
     out = {}
-    if handle.cfg.use_fp8:
+    if cfg.use_fp8:
         out["recv_x"] = mk((rows, H), dtype=torch.uint8, device="cuda")
-        out["recv_sf"] = mk((int(handle.info.sf_numel),), dtype=torch.float32, device="cuda")
+        out["recv_sf"] = mk((int(info.sf_numel),), dtype=torch.float32, device="cuda")
     else:
         out["recv_x"] = mk((rows, H), dtype=torch.bfloat16, device="cuda")
         out["recv_sf"] = None
     if with_weights:
-        shape = (rows,) if handle.cfg.do_expand else (rows, K)
+        shape = (rows,) if cfg.do_expand else (rows, K)
         out["recv_topk_weights"] = mk(shape, dtype=torch.float32, device="cuda")
     else:
         out["recv_topk_weights"] = None
-    if with_idx and not handle.cfg.do_expand:
+    if with_idx and not cfg.do_expand:
         out["recv_topk_idx"] = mk((rows, K), dtype=torch.int32, device="cuda")
     else:
         out["recv_topk_idx"] = None
     return out
+
+
+def alloc_recv(handle: Handle, with_weights: bool = False, with_idx: bool = False,
+               zero: bool = False) -> dict:
+    """Allocate the dispatch outputs for ``handle`` with torch (device memory only)."""
+    return _alloc(handle.cfg, handle.info, with_weights, with_idx, zero)
+
+
+def plan_layout(cfg: EpConfigC) -> EpLayoutInfoC:
+    """Sizes of a do_cpu_sync = 0 layout (ep_plan_layout), before any GPU work."""
+    info = EpLayoutInfoC()
+    st = load_library().ep_plan_layout(ctypes.byref(cfg), ctypes.byref(info))
+    if st != EP_OK:
+        raise EpError(st, "ep_plan_layout")
+    return info
+
+
+def alloc_recv_planned(cfg: EpConfigC, with_weights: bool = False, with_idx: bool = False,
+                       zero: bool = False) -> dict:
+    """Allocate the dispatch outputs of a do_cpu_sync = 0 configuration from its plan."""
+    return _alloc(cfg, plan_layout(cfg), with_weights, with_idx, zero)
+
+
+def ep_layout_dispatch(cfg: EpConfigC, topk_idx: torch.Tensor, x: torch.Tensor,
+                       topk_weights: Optional[torch.Tensor], recv_x: torch.Tensor,
+                       recv_sf: Optional[torch.Tensor] = None,
+                       recv_topk_weights: Optional[torch.Tensor] = None,
+                       recv_topk_idx: Optional[torch.Tensor] = None, stream=None) -> Handle:
+    """Layout and dispatch in one call (ep_layout_dispatch); returns the handle."""
+    lib = load_library()
+    if topk_idx.dtype not in (torch.int64, torch.int32):
+        raise ValueError("topk_idx must be int64 or int32")
+    if tuple(topk_idx.shape) != (cfg.num_tokens, cfg.num_topk):
+        raise ValueError(f"topk_idx shape {tuple(topk_idx.shape)} != "
+                         f"({cfg.num_tokens}, {cfg.num_topk})")
+    if tuple(x.shape) != (cfg.num_tokens, cfg.hidden):
+        raise ValueError(f"x shape {tuple(x.shape)} != ({cfg.num_tokens}, {cfg.hidden})")
+    cfg.topk_idx_is_int64 = 1 if topk_idx.dtype == torch.int64 else 0
+    h = ctypes.c_void_p(0)
+    info = EpLayoutInfoC()
+    st = lib.ep_layout_dispatch(
+        ctypes.byref(cfg), _ptr(topk_idx, "topk_idx"), _ptr(x, "x", torch.bfloat16),
+        _ptr(topk_weights, "topk_weights", torch.float32),
+        _ptr(recv_x, "recv_x", (torch.bfloat16, torch.uint8, torch.float8_e4m3fn)),
+        _ptr(recv_sf, "recv_sf", torch.float32),
+        _ptr(recv_topk_weights, "recv_topk_weights", torch.float32),
+        _ptr(recv_topk_idx, "recv_topk_idx", torch.int32), _stream_ptr(stream),
+        ctypes.byref(h), ctypes.byref(info))
+    if st != EP_OK:
+        raise EpError(st, "ep_layout_dispatch")
+    return Handle(h.value, EpConfigC.from_buffer_copy(cfg), info, st)
 
 
 def ep_dispatch(handle: Handle, x: torch.Tensor, topk_weights: Optional[torch.Tensor],

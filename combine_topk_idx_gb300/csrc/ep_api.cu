@@ -363,26 +363,73 @@ ep_status ep_host_wait_flag(const volatile int32_t *flag, int32_t expected, int3
   }
 }
 
-ep_status ep_layout(const ep_config *cfg, const void *topk_idx, ep_stream_t stream,
-                    ep_handle **out_handle, ep_layout_info *info) {
-  if (out_handle == nullptr || info == nullptr) return EP_ERR_INVALID_ARG;
-  *out_handle = nullptr;
+namespace ep {
+namespace {
+
+// Scale-factor strides and size of a handle with `rows_alloc` receive rows.
+void plan_sf(const ep_config &c, int64_t rows_alloc, int64_t fixed_cap, int64_t *token_stride,
+             int64_t *hidden_stride, int64_t *numel, int64_t *expert_stride) {
+  const int64_t nb = c.hidden / kFp8Block;
+  *expert_stride = 0;
+  if (c.use_fp8 && c.fixed_capacity) {
+    if (c.use_tma_aligned_col_major_sf) {  // one column-major slab per expert
+      *token_stride = 1;
+      *hidden_stride = align_up(fixed_cap, 4);
+      *expert_stride = nb * *hidden_stride;
+    } else {
+      *token_stride = nb;
+      *hidden_stride = 1;
+      *expert_stride = nb * fixed_cap;
+    }
+    *numel = (int64_t)c.num_experts * *expert_stride;
+  } else if (c.use_fp8) {
+    if (c.use_tma_aligned_col_major_sf) {
+      *token_stride = 1;
+      *hidden_stride = align_up(rows_alloc, 4);
+      *numel = nb * *hidden_stride;
+    } else {
+      *token_stride = nb;
+      *hidden_stride = 1;
+      *numel = nb * rows_alloc;
+    }
+  } else {
+    *token_stride = *hidden_stride = *numel = 0;
+  }
+}
+
+// Everything of a layout up to its launch: checks, the layout parameters and
+// the handle's device block (stream-ordered on s).
+struct LayoutSetup {
+  ep_config c;
+  cudaStream_t s;
+  bool capturing;
+  int dev;
+  Bounds b;
+  LayoutParams lp;
+  void *dmem;
+  float *tok_scale;
+};
+
+ep_status layout_setup(const ep_config *cfg, const void *topk_idx, ep_stream_t stream,
+                       LayoutSetup *L) {
   ep_status st = ep_validate_config(cfg);
   if (st != EP_OK) return st;
   const ep_config c = *cfg;
+  L->c = c;
   const int T = c.num_tokens, K = c.num_topk, E = c.num_experts, R = c.num_ranks;
   if (T > 0 && (topk_idx == nullptr || !aligned(topk_idx, c.topk_idx_is_int64 ? 8 : 4)))
     return EP_ERR_INVALID_ARG;
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  L->s = s;
   cudaStreamCaptureStatus cs = cudaStreamCaptureStatusNone;
   if (cudaStreamIsCapturing(s, &cs) != cudaSuccess) return EP_ERR_CUDA;
-  const bool capturing = cs != cudaStreamCaptureStatusNone;
-  if (c.do_cpu_sync && capturing) return EP_ERR_INVALID_ARG;
-  int dev = 0;
-  if (cudaGetDevice(&dev) != cudaSuccess) return EP_ERR_CUDA;
+  L->capturing = cs != cudaStreamCaptureStatusNone;
+  if (c.do_cpu_sync && L->capturing) return EP_ERR_INVALID_ARG;
+  if (cudaGetDevice(&L->dev) != cudaSuccess) return EP_ERR_CUDA;
 
-  const ep::Bounds b = ep::upper_bound(c);
-  ep::LayoutParams lp{};
+  const Bounds b = upper_bound(c);
+  L->b = b;
+  LayoutParams lp{};
   lp.topk_idx = topk_idx;
   lp.idx_is_int64 = c.topk_idx_is_int64;
   lp.T = T; lp.K = K; lp.E = E; lp.R = R; lp.L = E / R;
@@ -394,7 +441,7 @@ ep_status ep_layout(const ep_config *cfg, const void *topk_idx, ep_stream_t stre
   // past the allocation are dropped and flagged
   lp.row_limit = c.do_cpu_sync ? b.global : b.rows;
   // Chunks of up to 256 tokens that never straddle a source rank.
-  lp.chunk_tokens = ep::kLayoutChunkTokens;
+  lp.chunk_tokens = kLayoutChunkTokens;
   const int TB = lp.chunk_tokens;
   const int64_t src_ranks = ((int64_t)T + lp.M - 1) / lp.M;
   const int64_t max_tok = std::min<int64_t>(lp.M, T);
@@ -402,8 +449,8 @@ ep_status ep_layout(const ep_config *cfg, const void *topk_idx, ep_stream_t stre
   const int64_t nblocks = std::max<int64_t>(1, src_ranks * lp.blocks_per_src);
   if (nblocks > 0x7fffffff) return EP_ERR_UNSUPPORTED;
   lp.num_blocks = (int)nblocks;
-  lp.rank_warps = ep::layout_rank_warps(c.do_expand ? E : R);
-  if (ep::layout_assign_smem(lp) > 220 * 1024) return EP_ERR_UNSUPPORTED;
+  lp.rank_warps = layout_rank_warps(c.do_expand ? E : R);
+  if (layout_assign_smem(lp) > 220 * 1024) return EP_ERR_UNSUPPORTED;
 
   // One device block, carved into 256-byte aligned arrays.
   size_t off = 0;
@@ -412,8 +459,8 @@ ep_status ep_layout(const ep_config *cfg, const void *topk_idx, ep_stream_t stre
     off += (bytes + 255) / 256 * 256;
     return o;
   };
-  const size_t o_ctrl = take(sizeof(int32_t) * ep::kCtrlWords);
-  const size_t o_sync = take(sizeof(int32_t) * ep::kDispSyncWords);
+  const size_t o_ctrl = take(sizeof(int32_t) * kCtrlWords);
+  const size_t o_sync = take(sizeof(int32_t) * kDispSyncWords);
   const size_t o_topk = take(sizeof(int32_t) * (size_t)T * K);
   const size_t o_dst = take(sizeof(int32_t) * (size_t)T * K);
   const size_t o_meta = take(sizeof(int32_t) * 2 * (size_t)lp.row_limit);
@@ -428,18 +475,18 @@ ep_status ep_layout(const ep_config *cfg, const void *topk_idx, ep_stream_t stre
   const size_t o_blke = take(sizeof(int32_t) * (size_t)E * lp.num_blocks);
   const size_t o_blkr = take(sizeof(int32_t) * (size_t)R * lp.num_blocks);
   const size_t o_blkerr = take(sizeof(uint32_t) * (size_t)lp.num_blocks);
-  const size_t o_toks = take(c.use_fp8 ? sizeof(float) * (size_t)T * (c.hidden / ep::kFp8Block) : 0);
+  const size_t o_toks = take(c.use_fp8 ? sizeof(float) * (size_t)T * (c.hidden / kFp8Block) : 0);
   void *dmem = nullptr;
   cudaError_t ce;
-  if (capturing) {
+  if (L->capturing) {
     // inside a stream capture the allocation becomes a graph memory node
     ce = cudaMallocAsync(&dmem, off, s);
   } else {
     cudaMemPool_t pool = nullptr;
-    ce = ep::handle_pool(dev, &pool);
+    ce = handle_pool(L->dev, &pool);
     if (ce == cudaSuccess) ce = cudaMallocFromPoolAsync(&dmem, off, pool, s);
   }
-  if (ce != cudaSuccess) return ep::cuda_status(ce);
+  if (ce != cudaSuccess) return cuda_status(ce);
   uint8_t *base = static_cast<uint8_t *>(dmem);
   lp.ctrl = reinterpret_cast<int32_t *>(base + o_ctrl);
   lp.disp_sync = reinterpret_cast<int32_t *>(base + o_sync);
@@ -457,85 +504,32 @@ ep_status ep_layout(const ep_config *cfg, const void *topk_idx, ep_stream_t stre
   lp.blk_e = reinterpret_cast<int32_t *>(base + o_blke);
   lp.blk_r = reinterpret_cast<int32_t *>(base + o_blkr);
   lp.blk_err = reinterpret_cast<uint32_t *>(base + o_blkerr);
-  float *tok_scale = c.use_fp8 ? reinterpret_cast<float *>(base + o_toks) : nullptr;
+  L->tok_scale = c.use_fp8 ? reinterpret_cast<float *>(base + o_toks) : nullptr;
+  L->lp = lp;
+  L->dmem = dmem;
+  return EP_OK;
+}
 
-  auto fail = [&](ep_status code) {
-    cudaFreeAsync(dmem, s);
-    return code;
-  };
-
-  ep::SyncPool::Slot slot{nullptr, nullptr};
-  if (c.do_cpu_sync) {
-    int32_t seq = 0;
-    if (!ep::sync_pool().acquire(&seq, &slot)) return fail(EP_ERR_OOM);
-    slot.host->num_recv = slot.host->num_expanded = slot.host->error = 0;
-    lp.host = slot.dev;
-    lp.seq = seq;
-  }
-  ce = ep::launch_layout(lp, s);
-  if (ce != cudaSuccess) {
-    // the kernel may not have run: the slot is not safe to hand out again
-    return fail(ep::cuda_status(ce));
-  }
-
+// The handle of a launched layout with `rows_alloc` receive rows.
+ep_handle *make_handle(const LayoutSetup &L, int64_t rows_alloc) {
   ep_handle *h = new ep_handle();
-  h->cfg = c;
-  h->device = dev;
-  h->stream = s;
-  h->dmem = dmem;
-  h->lp = lp;
+  h->cfg = L.c;
+  h->device = L.dev;
+  h->stream = L.s;
+  h->dmem = L.dmem;
+  h->lp = L.lp;
   h->lp.host = nullptr;
   h->lp.topk_idx = nullptr;
-  h->tok_scale = tok_scale;
+  h->tok_scale = L.tok_scale;
+  h->rows_alloc = rows_alloc;
+  plan_sf(L.c, rows_alloc, L.lp.fixed_cap, &h->sf_token_stride, &h->sf_hidden_stride,
+          &h->sf_numel, &h->sf_expert_stride);
+  return h;
+}
 
-  st = EP_OK;
-  int64_t num_recv = -1, num_exp = -1;
-  if (c.do_cpu_sync) {
-    const int32_t timeout = c.cpu_sync_timeout_ms > 0 ? c.cpu_sync_timeout_ms : 10000;
-    uint64_t words[3];
-    const ep_status w = ep::wait_host_words(slot.host, lp.seq, timeout, words);
-    if (w != EP_OK) {
-      // the slot may still be written later: leave it out of the pool
-      delete h;
-      return fail(w);
-    }
-    num_recv = (uint32_t)words[0];
-    num_exp = (uint32_t)words[1];
-    const uint32_t err = (uint32_t)words[2];
-    ep::sync_pool().release(slot);
-    h->rows_alloc = c.fixed_capacity ? b.rows : c.do_expand ? num_exp : num_recv;
-    if (err & EP_ERRBIT_BAD_TOPK_IDX) st = EP_ERR_BAD_TOPK_IDX;
-  } else {
-    h->rows_alloc = b.rows;
-  }
-  const int64_t nb = c.hidden / ep::kFp8Block;
-  h->sf_expert_stride = 0;
-  if (c.use_fp8 && c.fixed_capacity) {
-    const int64_t cap = lp.fixed_cap;
-    if (c.use_tma_aligned_col_major_sf) {  // one column-major slab per expert
-      h->sf_token_stride = 1;
-      h->sf_hidden_stride = align_up(cap, 4);
-      h->sf_expert_stride = nb * h->sf_hidden_stride;
-    } else {
-      h->sf_token_stride = nb;
-      h->sf_hidden_stride = 1;
-      h->sf_expert_stride = nb * cap;
-    }
-    h->sf_numel = (int64_t)c.num_experts * h->sf_expert_stride;
-  } else if (c.use_fp8) {
-    if (c.use_tma_aligned_col_major_sf) {
-      h->sf_token_stride = 1;
-      h->sf_hidden_stride = align_up(h->rows_alloc, 4);
-      h->sf_numel = nb * h->sf_hidden_stride;
-    } else {
-      h->sf_token_stride = nb;
-      h->sf_hidden_stride = 1;
-      h->sf_numel = nb * h->rows_alloc;
-    }
-  } else {
-    h->sf_token_stride = h->sf_hidden_stride = h->sf_numel = 0;
-  }
-
+void fill_info(const ep_handle *h, int64_t num_recv, int64_t num_exp, int layout_kernels,
+               ep_layout_info *info) {
+  const LayoutParams &lp = h->lp;
   info->num_recv_tokens = num_recv;
   info->num_expanded_tokens = num_exp;
   info->rows_alloc = h->rows_alloc;
@@ -552,25 +546,102 @@ ep_status ep_layout(const ep_config *cfg, const void *topk_idx, ep_stream_t stre
   info->dst_buffer_slot_idx = lp.dst;
   info->recv_src_metadata = lp.meta;
   info->is_token_in_rank = lp.in_rank;
-  info->totals = lp.ctrl + ep::kCtrlNumRecv;
-  info->error_word = reinterpret_cast<const uint32_t *>(lp.ctrl + ep::kCtrlError);
+  info->totals = lp.ctrl + kCtrlNumRecv;
+  info->error_word = reinterpret_cast<const uint32_t *>(lp.ctrl + kCtrlError);
   info->meta_rows = lp.row_limit;
   info->expert_capacity = lp.fixed_cap;
   info->sf_expert_stride = h->sf_expert_stride;
+  info->layout_kernels = layout_kernels;
+  info->reserved1 = 0;
+}
+
+}  // namespace
+}  // namespace ep
+
+ep_status ep_layout(const ep_config *cfg, const void *topk_idx, ep_stream_t stream,
+                    ep_handle **out_handle, ep_layout_info *info) {
+  if (out_handle == nullptr || info == nullptr) return EP_ERR_INVALID_ARG;
+  *out_handle = nullptr;
+  ep::LayoutSetup L;
+  ep_status st = ep::layout_setup(cfg, topk_idx, stream, &L);
+  if (st != EP_OK) return st;
+  const ep_config &c = L.c;
+  ep::LayoutParams &lp = L.lp;
+  auto fail = [&](ep_status code) {
+    cudaFreeAsync(L.dmem, L.s);
+    return code;
+  };
+
+  ep::SyncPool::Slot slot{nullptr, nullptr};
+  if (c.do_cpu_sync) {
+    int32_t seq = 0;
+    if (!ep::sync_pool().acquire(&seq, &slot)) return fail(EP_ERR_OOM);
+    slot.host->num_recv = slot.host->num_expanded = slot.host->error = 0;
+    lp.host = slot.dev;
+    lp.seq = seq;
+  }
+  int layout_kernels = 0;
+  const cudaError_t ce = ep::launch_layout(lp, L.s, &layout_kernels);
+  if (ce != cudaSuccess) {
+    // the kernel may not have run: the slot is not safe to hand out again
+    return fail(ep::cuda_status(ce));
+  }
+
+  st = EP_OK;
+  int64_t num_recv = -1, num_exp = -1;
+  int64_t rows_alloc = L.b.rows;
+  if (c.do_cpu_sync) {
+    const int32_t timeout = c.cpu_sync_timeout_ms > 0 ? c.cpu_sync_timeout_ms : 10000;
+    uint64_t words[3];
+    const ep_status w = ep::wait_host_words(slot.host, lp.seq, timeout, words);
+    if (w != EP_OK) {
+      // the slot may still be written later: leave it out of the pool
+      return fail(w);
+    }
+    num_recv = (uint32_t)words[0];
+    num_exp = (uint32_t)words[1];
+    const uint32_t err = (uint32_t)words[2];
+    ep::sync_pool().release(slot);
+    rows_alloc = c.fixed_capacity ? L.b.rows : c.do_expand ? num_exp : num_recv;
+    if (err & EP_ERRBIT_BAD_TOPK_IDX) st = EP_ERR_BAD_TOPK_IDX;
+  }
+  ep_handle *h = ep::make_handle(L, rows_alloc);
+  ep::fill_info(h, num_recv, num_exp, layout_kernels, info);
   *out_handle = h;
   return st;
 }
 
-ep_status ep_dispatch(ep_handle *h, const void *x, const float *topk_weights, void *recv_x,
-                      float *recv_sf, float *recv_topk_weights, int32_t *recv_topk_idx,
-                      ep_stream_t stream) {
-  if (h == nullptr) return EP_ERR_INVALID_ARG;
-  const ep_config &c = h->cfg;
+ep_status ep_plan_layout(const ep_config *cfg, ep_layout_info *info) {
+  if (info == nullptr) return EP_ERR_INVALID_ARG;
+  const ep_status st = ep_validate_config(cfg);
+  if (st != EP_OK) return st;
+  if (cfg->do_cpu_sync) return EP_ERR_INVALID_ARG;  // sizes depend on the routing
+  const ep::Bounds b = ep::upper_bound(*cfg);
+  const int64_t fixed_cap =
+      cfg->fixed_capacity ? (int64_t)cfg->num_max_tokens_per_rank * cfg->num_ranks : 0;
+  *info = ep_layout_info{};
+  info->num_recv_tokens = info->num_expanded_tokens = -1;
+  info->rows_alloc = b.rows;
+  ep::plan_sf(*cfg, b.rows, fixed_cap, &info->sf_token_stride, &info->sf_hidden_stride,
+              &info->sf_numel, &info->sf_expert_stride);
+  info->meta_rows = b.rows;
+  info->expert_capacity = fixed_cap;
+  return EP_OK;
+}
+
+namespace ep {
+namespace {
+
+// Pointer checks of a quantising / BF16 dispatch into `rows_alloc` rows.
+ep_status check_dispatch_args(const ep_config &c, int64_t rows_alloc, const void *x,
+                              const float *topk_weights, const void *recv_x,
+                              const float *recv_sf, const float *recv_topk_weights,
+                              const int32_t *recv_topk_idx) {
   const int T = c.num_tokens;
   if (T > 0 && (x == nullptr || !aligned(x, 16))) return EP_ERR_INVALID_ARG;
-  if (h->rows_alloc > 0 && (recv_x == nullptr || !aligned(recv_x, 16))) return EP_ERR_INVALID_ARG;
+  if (rows_alloc > 0 && (recv_x == nullptr || !aligned(recv_x, 16))) return EP_ERR_INVALID_ARG;
   if (c.use_fp8) {
-    if (h->rows_alloc > 0 && (recv_sf == nullptr || !aligned(recv_sf, 4))) return EP_ERR_INVALID_ARG;
+    if (rows_alloc > 0 && (recv_sf == nullptr || !aligned(recv_sf, 4))) return EP_ERR_INVALID_ARG;
   } else if (recv_sf != nullptr) {
     return EP_ERR_INVALID_ARG;
   }
@@ -580,6 +651,21 @@ ep_status ep_dispatch(ep_handle *h, const void *x, const float *topk_weights, vo
   if (topk_weights != nullptr && !aligned(topk_weights, 4)) return EP_ERR_INVALID_ARG;
   if (recv_topk_idx != nullptr && (c.do_expand || !aligned(recv_topk_idx, 4)))
     return EP_ERR_INVALID_ARG;
+  return EP_OK;
+}
+
+}  // namespace
+}  // namespace ep
+
+ep_status ep_dispatch(ep_handle *h, const void *x, const float *topk_weights, void *recv_x,
+                      float *recv_sf, float *recv_topk_weights, int32_t *recv_topk_idx,
+                      ep_stream_t stream) {
+  if (h == nullptr) return EP_ERR_INVALID_ARG;
+  const ep_config &c = h->cfg;
+  if (const ep_status st = ep::check_dispatch_args(c, h->rows_alloc, x, topk_weights, recv_x,
+                                                   recv_sf, recv_topk_weights, recv_topk_idx);
+      st != EP_OK)
+    return st;
   if (const ep_status st = ep::check_device(h); st != EP_OK) return st;
   const ep::DispatchParams p = ep::dispatch_params(h, x, topk_weights, recv_x, recv_sf,
                                                    recv_topk_weights, recv_topk_idx);
@@ -588,6 +674,44 @@ ep_status ep_dispatch(ep_handle *h, const void *x, const float *topk_weights, vo
       ep::launch_dispatch(p, c.use_fp8, c.use_tma_aligned_col_major_sf, c.num_sms,
                           reinterpret_cast<cudaStream_t>(stream));
   return ep::cuda_status(ce);
+}
+
+ep_status ep_layout_dispatch(const ep_config *cfg, const void *topk_idx, const void *x,
+                             const float *topk_weights, void *recv_x, float *recv_sf,
+                             float *recv_topk_weights, int32_t *recv_topk_idx,
+                             ep_stream_t stream, ep_handle **out_handle, ep_layout_info *info) {
+  if (out_handle == nullptr || info == nullptr) return EP_ERR_INVALID_ARG;
+  *out_handle = nullptr;
+  if (cfg == nullptr) return EP_ERR_INVALID_ARG;
+  if (cfg->do_cpu_sync) return EP_ERR_INVALID_ARG;  // receive buffers are sized in advance
+  if (const ep_status st = ep_validate_config(cfg); st != EP_OK) return st;
+  if (const ep_status st =
+          ep::check_dispatch_args(*cfg, ep::upper_bound(*cfg).rows, x, topk_weights, recv_x,
+                                  recv_sf, recv_topk_weights, recv_topk_idx);
+      st != EP_OK)
+    return st;
+  ep::LayoutSetup L;
+  if (const ep_status st = ep::layout_setup(cfg, topk_idx, stream, &L); st != EP_OK) return st;
+  ep_handle *h = ep::make_handle(L, L.b.rows);
+  ep::DispatchParams p = ep::dispatch_params(h, x, topk_weights, recv_x, recv_sf,
+                                             recv_topk_weights, recv_topk_idx);
+  const ep_config &c = L.c;
+  int layout_kernels = 0;
+  // x is an input of this call, so it was complete before the layout
+  // started: the dispatch, launched right behind the layout, loads (and
+  // quantises) its first source rows while the layout runs
+  cudaError_t ce = ep::launch_layout(L.lp, L.s, &layout_kernels);
+  p.early_x = 1;
+  if (ce == cudaSuccess && h->rows_alloc > 0)
+    ce = ep::launch_dispatch(p, c.use_fp8, c.use_tma_aligned_col_major_sf, c.num_sms, L.s);
+  if (ce != cudaSuccess) {
+    cudaFreeAsync(L.dmem, L.s);
+    delete h;
+    return ep::cuda_status(ce);
+  }
+  ep::fill_info(h, -1, -1, layout_kernels, info);
+  *out_handle = h;
+  return EP_OK;
 }
 
 ep_status ep_dispatch_fp8(ep_handle *h, const void *x_fp8, const float *x_sf,

@@ -169,7 +169,8 @@ __global__ void __launch_bounds__(kMaxConsumers + 32, 1) dispatch_kernel(Dispatc
   constexpr bool FP8 = MODE == kModeQuant;         // quantise in the consumers
   constexpr bool FP8_OUT = MODE != kModeBf16;      // e4m3 payload + scales
   extern __shared__ __align__(128) uint8_t smem[];
-  __shared__ __align__(8) uint64_t full[S];
+  __shared__ __align__(8) uint64_t full[S];    // source row landed (and meta[s].t set)
+  __shared__ __align__(8) uint64_t rows[S];    // row list of the stage written
   __shared__ __align__(8) uint64_t empty[S];
   __shared__ TokenMeta meta[S];
   __shared__ int prow_s[2][kPadRowsPerItem];
@@ -190,32 +191,45 @@ __global__ void __launch_bounds__(kMaxConsumers + 32, 1) dispatch_kernel(Dispatc
   if (threadIdx.x == 0) {
     for (int s = 0; s < S; ++s) {
       mbar_init(&full[s], 1);
+      mbar_init(&rows[s], 1);
       mbar_init(&empty[s], ncw);
     }
     fence_mbar_init();
   }
   __syncthreads();
-  // Launched with programmatic dependent launch: the set-up above overlaps
-  // the tail of the kernel before this one; nothing below touches global
-  // memory before that kernel's writes are visible.
-  griddep_wait();
 
   // x rows and the destination payload are touched once: evict them first so
   // that the small, scattered scale-factor sectors stay in L2 until complete.
   const uint64_t stream_pol = l2_policy_evict_first();
+  auto issue_row = [&](int s, int t) {  // lane 0 of the producer
+    meta[s].t = t;
+    mbar_arrive_expect_tx(&full[s], (uint32_t)in_bytes);
+    const void *src = MODE == kModePreq ? static_cast<const void *>(p.xq + (int64_t)t * H)
+                                        : static_cast<const void *>(p.x + (int64_t)t * H);
+    bulk_load_g2s_hint(in0 + s * in_stage, src, (uint32_t)in_bytes, &full[s], stream_pol);
+  };
   if (warp == 0) {
     // ---------------- producer ----------------
-    // The first token of each CTA is its index; the rest are handed out
-    // dynamically from a handle counter, so CTAs that run faster take more of
-    // them.  The next token and its routing are fetched while the current
-    // one is issued.
+    // CTA b's first S tokens are b, b + G, ..., b + (S - 1) G; the rest are
+    // handed out dynamically from a handle counter, so CTAs that run faster
+    // take more of them.  The next token and its routing are fetched while
+    // the current one is issued.
     const int G = gridDim.x;
+    // Launched with programmatic dependent launch: everything above overlaps
+    // the tail of the kernel before this one.  The first S source rows need
+    // no output of that kernel; with early_x their loads leave before the
+    // wait.  Nothing below the wait reads global memory before that kernel's
+    // writes are visible.
+    const int64_t early = p.early_x ? S : 0;
+    if (lane == 0)
+      for (int k = 0; k < early && blockIdx.x + (int64_t)k * G < p.T; ++k)
+        issue_row(k, (int)(blockIdx.x + (int64_t)k * G));
+    griddep_wait();
     int next = blockIdx.x;
     Routing rn{-1, -1, 0.f};
     if (next < p.T) rn = load_routing(p, next, lane);
     for (int64_t i = 0;; ++i) {
       const int t = next;
-      const Routing cur = rn;
       const int s = (int)(i % S);
       const int64_t k = i / S;
       if (k > 0) {
@@ -235,16 +249,14 @@ __global__ void __launch_bounds__(kMaxConsumers + 32, 1) dispatch_kernel(Dispatc
         }
         break;
       }
-      // The source row first: its load needs only the token index, so it
-      // overlaps the ticket for the next token and the routing work below.
-      // The stage completes once its bytes have landed and the producer has
-      // arrived after writing the row list.
+      const Routing cur = rn;
+      // The source row first (unless it left before the wait): its load
+      // needs only the token index, so it overlaps the ticket for the next
+      // token and the routing work below.
       if (lane == 0) {
-        mbar_expect_tx(&full[s], (uint32_t)in_bytes);
-        const void *src = MODE == kModePreq ? static_cast<const void *>(p.xq + (int64_t)t * H)
-                                            : static_cast<const void *>(p.x + (int64_t)t * H);
-        bulk_load_g2s_hint(in0 + s * in_stage, src, (uint32_t)in_bytes, &full[s], stream_pol);
-        next = G + atomicAdd(p.sched, 1);
+        if (i >= early) issue_row(s, t);
+        next = i + 1 < S ? (int)min((int64_t)p.T, blockIdx.x + (i + 1) * (int64_t)G)
+                         : S * G + atomicAdd(p.sched, 1);
       }
       const unsigned peers = __match_any_sync(0xffffffffu, cur.d);
       const bool keep = cur.d >= 0 && lane == __ffs(peers) - 1;
@@ -275,7 +287,7 @@ __global__ void __launch_bounds__(kMaxConsumers + 32, 1) dispatch_kernel(Dispatc
         }
       }
       __syncwarp();
-      if (lane == 0) mbar_arrive(&full[s]);
+      if (lane == 0) mbar_arrive(&rows[s]);
       next = __shfl_sync(0xffffffffu, next, 0);
       if (next < p.T) rn = load_routing(p, next, lane);
     }
@@ -286,10 +298,10 @@ __global__ void __launch_bounds__(kMaxConsumers + 32, 1) dispatch_kernel(Dispatc
   const int ctid = threadIdx.x - 32;
   const int nct = blockDim.x - 32;
   const int nvec = H / 8;  // 16-byte vectors of the BF16 row
-  const bool pad_work = p.do_expand && (p.zero_padding || p.recv_w != nullptr);
-  const int npad = pad_work ? __ldg(p.psum_pad + p.E) : 0;
-  const int64_t pad_items = (npad + kPadRowsPerItem - 1) / kPadRowsPerItem;
   uint8_t *recv = static_cast<uint8_t *>(p.recv_x);
+  // Quantising a row needs only the row itself; its row list (the layout's
+  // output) is read after the wait.
+  bool waited = false;
   // row-major scale stores: when nb divides the consumer count, thread ctid
   // owns scale column ctid % nb of rows ctid / nb, + nct / nb, ...
   const int sf_step = (nb > 0 && nct % nb == 0) ? nct / nb : 0;
@@ -298,90 +310,100 @@ __global__ void __launch_bounds__(kMaxConsumers + 32, 1) dispatch_kernel(Dispatc
   for (int64_t i = 0;; ++i) {
     const int s = (int)(i % S);
     const uint32_t par = (uint32_t)((i / S) & 1);
-    if (!mbar_wait_bounded(&full[s], par, kWaitIters, kWaitHintNs)) {
+    auto wait_or_fail = [&](uint64_t *bar) {
+      if (mbar_wait_bounded(bar, par, kWaitIters, kWaitHintNs)) return true;
+      if (!waited) griddep_wait();
       if (lane == 0) atomicOr(p.err, EP_ERRBIT_TIMEOUT);
       if (ctid == 0) bulk_wait_all<0>();
-      return;
-    }
+      return false;
+    };
+    if (!wait_or_fail(&full[s])) return;
     const int t = meta[s].t;
     if (t < 0) break;  // the producer has no more tokens
-    const int n = meta[s].n;
     const uint8_t *in = in0 + s * in_stage;
     if constexpr (FP8) {
       uint8_t *out = out0 + s * out_stage;
       float *sf = sf0 + s * nb_pad;
-      if (n > 0) {
-        // out stage s no longer read: at most S - 1 later bulk groups pending
-        if (ctid == 0) bulk_wait_read<S - 1>();
-        named_barrier(kBarConsumers, nct);
-        // every consumer thread runs the same number of iterations so the
-        // 16-lane shuffles always see full warps (nvec and nct are multiples of 16)
-        for (int v0 = 0; v0 < nvec; v0 += nct) {
-          const int v = v0 + ctid;
-          const bool valid = v < nvec;
-          const uint4 x8 = valid ? *reinterpret_cast<const uint4 *>(in + v * 16)
-                                 : make_uint4(0, 0, 0, 0);
-          float f[8];
-          f[0] = bf16_lo(x8.x); f[1] = bf16_hi(x8.x);
-          f[2] = bf16_lo(x8.y); f[3] = bf16_hi(x8.y);
-          f[4] = bf16_lo(x8.z); f[5] = bf16_hi(x8.z);
-          f[6] = bf16_lo(x8.w); f[7] = bf16_hi(x8.w);
-          // amax propagates NaN (max.NaN): a block holding a NaN gets a NaN
-          // scale and the NaN code 0x7F in every byte
-          float amax = 0.f;
+      // out stage s no longer read: at most S - 1 later bulk groups pending
+      if (ctid == 0) bulk_wait_read<S - 1>();
+      named_barrier(kBarConsumers, nct);
+      // every consumer thread runs the same number of iterations so the
+      // 16-lane shuffles always see full warps (nvec and nct are multiples of 16)
+      for (int v0 = 0; v0 < nvec; v0 += nct) {
+        const int v = v0 + ctid;
+        const bool valid = v < nvec;
+        const uint4 x8 = valid ? *reinterpret_cast<const uint4 *>(in + v * 16)
+                               : make_uint4(0, 0, 0, 0);
+        float f[8];
+        f[0] = bf16_lo(x8.x); f[1] = bf16_hi(x8.x);
+        f[2] = bf16_lo(x8.y); f[3] = bf16_hi(x8.y);
+        f[4] = bf16_lo(x8.z); f[5] = bf16_hi(x8.z);
+        f[6] = bf16_lo(x8.w); f[7] = bf16_hi(x8.w);
+        // amax propagates NaN (max.NaN): a block holding a NaN gets a NaN
+        // scale and the NaN code 0x7F in every byte
+        float amax = 0.f;
 #pragma unroll
-          for (int q = 0; q < 8; ++q) amax = fmax_nan(amax, fabsf(f[q]));
-          // 16 consecutive lanes hold one 128-element block
-          amax = fmax_nan(amax, __shfl_xor_sync(0xffffffffu, amax, 1));
-          amax = fmax_nan(amax, __shfl_xor_sync(0xffffffffu, amax, 2));
-          amax = fmax_nan(amax, __shfl_xor_sync(0xffffffffu, amax, 4));
-          amax = fmax_nan(amax, __shfl_xor_sync(0xffffffffu, amax, 8));
-          if (valid) {
-            const float sc = __fdiv_rn(amax, 448.0f);
-            uint2 packed = make_uint2(0, 0);
-            if (amax != amax) {
-              packed = make_uint2(0x7F7F7F7Fu, 0x7F7F7F7Fu);
-            } else if (amax != 0.f) {
-              // an infinite amax: finite elements divide to +-0, infinite ones
-              // to NaN, which the conversion encodes as 0x7F
-              packed = e4m3_block8(f, sc);
-            }
-            *reinterpret_cast<uint2 *>(out + v * 8) = packed;
-            if ((v & 15) == 0) {
-              if (COL_MAJOR)
-                p.tok_scale[(int64_t)t * nb + (v >> 4)] = sc;
-              else
-                sf[v >> 4] = sc;
-            }
+        for (int q = 0; q < 8; ++q) amax = fmax_nan(amax, fabsf(f[q]));
+        // 16 consecutive lanes hold one 128-element block
+        amax = fmax_nan(amax, __shfl_xor_sync(0xffffffffu, amax, 1));
+        amax = fmax_nan(amax, __shfl_xor_sync(0xffffffffu, amax, 2));
+        amax = fmax_nan(amax, __shfl_xor_sync(0xffffffffu, amax, 4));
+        amax = fmax_nan(amax, __shfl_xor_sync(0xffffffffu, amax, 8));
+        if (valid) {
+          const float sc = __fdiv_rn(amax, 448.0f);
+          uint2 packed = make_uint2(0, 0);
+          if (amax != amax) {
+            packed = make_uint2(0x7F7F7F7Fu, 0x7F7F7F7Fu);
+          } else if (amax != 0.f) {
+            // an infinite amax: finite elements divide to +-0, infinite ones
+            // to NaN, which the conversion encodes as 0x7F
+            packed = e4m3_block8(f, sc);
+          }
+          *reinterpret_cast<uint2 *>(out + v * 8) = packed;
+          if ((v & 15) == 0) {
+            if (COL_MAJOR)
+              p.tok_scale[(int64_t)t * nb + (v >> 4)] = sc;
+            else
+              sf[v >> 4] = sc;
           }
         }
-        fence_proxy_async_smem();
-        named_barrier(kBarConsumers, nct);
-        if (ctid == 0) {
-          for (int r = 0; r < n; ++r)
-            bulk_store_s2g_hint(recv + (int64_t)meta[s].rows[r] * out_bytes, out, (uint32_t)out_bytes,
-                                stream_pol);
-          bulk_commit();
-        }
-        if (!COL_MAJOR) {  // row-major scales: nb contiguous floats per row
-          if (sf_step > 0) {  // every thread keeps its column sf_j, rows sf_r0, +sf_step, ...
-            for (int r = sf_r0; r < n; r += sf_step)
-              p.recv_sf[(int64_t)meta[s].rows[r] * nb + sf_j] = sf[sf_j];
-          } else {
-            for (int e = ctid; e < n * nb; e += nct) {
-              const int r = e / nb, j = e - r * nb;
-              p.recv_sf[(int64_t)meta[s].rows[r] * nb + j] = sf[j];
-            }
+      }
+      fence_proxy_async_smem();
+      if (!waited) {
+        griddep_wait();
+        waited = true;
+      }
+      if (!wait_or_fail(&rows[s])) return;
+      const int n = meta[s].n;
+      named_barrier(kBarConsumers, nct);
+      if (ctid == 0) {
+        for (int r = 0; r < n; ++r)
+          bulk_store_s2g_hint(recv + (int64_t)meta[s].rows[r] * out_bytes, out, (uint32_t)out_bytes,
+                              stream_pol);
+        bulk_commit();  // one bulk group per token (empty when n = 0) keeps the stage reuse exact
+      }
+      if (!COL_MAJOR) {  // row-major scales: nb contiguous floats per row
+        if (sf_step > 0) {  // every thread keeps its column sf_j, rows sf_r0, +sf_step, ...
+          for (int r = sf_r0; r < n; r += sf_step)
+            p.recv_sf[(int64_t)meta[s].rows[r] * nb + sf_j] = sf[sf_j];
+        } else {
+          for (int e = ctid; e < n * nb; e += nct) {
+            const int r = e / nb, j = e - r * nb;
+            p.recv_sf[(int64_t)meta[s].rows[r] * nb + j] = sf[j];
           }
         }
-      } else if (ctid == 0) {
-        bulk_commit();  // one (here empty) bulk group per token keeps the stage reuse count exact
       }
       __syncwarp();
       if (lane == 0) mbar_arrive(&empty[s]);
     } else {
       // BF16 or pre-quantised: the input stage is the payload; it is released
       // once its bulk stores have read it.
+      if (!waited) {
+        griddep_wait();
+        waited = true;
+      }
+      if (!wait_or_fail(&rows[s])) return;
+      const int n = meta[s].n;
       if (ctid == 0) {
         for (int r = 0; r < n; ++r)
           bulk_store_s2g_hint(recv + (int64_t)meta[s].rows[r] * out_bytes, in, (uint32_t)out_bytes,
@@ -401,6 +423,10 @@ __global__ void __launch_bounds__(kMaxConsumers + 32, 1) dispatch_kernel(Dispatc
       if (lane == 0) mbar_arrive(&empty[s]);
     }
   }
+  if (!waited) griddep_wait();  // a CTA without tokens
+  const bool pad_work = p.do_expand && (p.zero_padding || p.recv_w != nullptr);
+  const int npad = pad_work ? __ldg(p.psum_pad + p.E) : 0;
+  const int64_t pad_items = (npad + kPadRowsPerItem - 1) / kPadRowsPerItem;
   // The CTA's tokens are done: publish that their per-token scales are
   // written and let the scale gather launch.  Then the padding items.
   if constexpr (FP8 && COL_MAJOR) {

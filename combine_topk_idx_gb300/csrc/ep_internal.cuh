@@ -11,6 +11,11 @@ namespace ep {
 constexpr int kFp8Block = 128;          // 1x128 scale blocks
 constexpr int kLayoutThreads = 1024;     // assign kernel CTA
 constexpr int kLayoutChunkTokens = 256;  // tokens per layout chunk (<= 8192 slots with K <= 32)
+// Rank layouts of at most this many chunks run as one kernel whose grid is a
+// single thread-block cluster (above 8 CTAs: a non-portable cluster size), if
+// its shared memory fits kLayoutClusterSmem and the device can place it.
+constexpr int kLayoutClusterChunks = 16;
+constexpr size_t kLayoutClusterSmem = 96 * 1024;
 
 // Control words at the head of the handle's device block.
 enum CtrlSlot { kCtrlError = 0, kCtrlNumRecv = 2, kCtrlNumExpanded = 3, kCtrlWords = 8 };
@@ -106,6 +111,10 @@ struct DispatchParams {
   // finished, padding items handed out (the last CTA resets all three for
   // the next dispatch on the handle)
   int32_t *sched;
+  // 1: x was complete before the kernel launched just ahead of this one
+  // started (the layout of the same call), so the first rows of every CTA
+  // are loaded and quantised before griddepcontrol.wait
+  int early_x;
 };
 
 struct CombineParams {
@@ -135,7 +144,8 @@ struct CombineWeightsParams {
 constexpr size_t kDynSmemOptIn = 40 * 1024;
 
 // Launchers (return the first CUDA error, cudaSuccess otherwise).
-cudaError_t launch_layout(const LayoutParams &p, cudaStream_t s);
+// launch_layout sets *kernels to the number of kernels it launched.
+cudaError_t launch_layout(const LayoutParams &p, cudaStream_t s, int *kernels);
 size_t layout_assign_smem(const LayoutParams &p);
 int layout_rank_warps(int nkey);
 // mode: 0 BF16 copy, 1 quantise BF16 to e4m3 + scales, 2 copy a pre-quantised input

@@ -110,6 +110,8 @@ extern "C" ep_status ep_layout_noalloc(const ep_config *cfg, const void *topk_id
   lp.psum_rs = out->psum_rank_src;
   lp.ctrl = out->status;
   lp.host = nullptr;
-  const cudaError_t ce = ep::launch_layout(lp, reinterpret_cast<cudaStream_t>(stream));
+  int kernels = 0;
+  const cudaError_t ce =
+      ep::launch_layout(lp, reinterpret_cast<cudaStream_t>(stream), &kernels);
   return ce == cudaSuccess ? EP_OK : EP_ERR_CUDA;
 }

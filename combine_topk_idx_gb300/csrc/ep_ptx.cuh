@@ -244,6 +244,32 @@ __device__ __forceinline__ void griddep_launch_dependents() {
   asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
 }
 
+// ---- thread-block clusters ----
+// Split cluster barrier: every thread of every CTA in the cluster must arrive
+// (no thread may exit before its last wait).  release/acquire order the
+// shared-memory writes before the arrival against the reads after the wait.
+__device__ __forceinline__ void cluster_arrive_release() {
+  asm volatile("barrier.cluster.arrive.release.aligned;" ::: "memory");
+}
+__device__ __forceinline__ void cluster_arrive_relaxed() {
+  asm volatile("barrier.cluster.arrive.relaxed.aligned;" ::: "memory");
+}
+__device__ __forceinline__ void cluster_wait() {
+  asm volatile("barrier.cluster.wait.acquire.aligned;" ::: "memory");
+}
+
+// 32-bit load from the shared memory of CTA `cta` of this cluster, at the
+// offset that `local` (a shared::cta address of this CTA) has here.
+__device__ __forceinline__ int ld_cluster_s32(uint32_t local, uint32_t cta) {
+  int v;
+  asm volatile(
+      "{\n\t.reg .b32 ra;\n\tmapa.shared::cluster.u32 ra, %1, %2;\n\t"
+      "ld.shared::cluster.b32 %0, [ra];\n\t}"
+      : "=r"(v)
+      : "r"(local), "r"(cta));
+  return v;
+}
+
 __device__ __forceinline__ int ld_acquire_gpu(const int32_t *p) {
   int v;
   asm volatile("ld.acquire.gpu.global.b32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");

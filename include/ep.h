@@ -147,6 +147,9 @@ typedef struct ep_layout_info {
   int64_t sf_expert_stride;           /* fixed_capacity: the scales of row e * capacity + i
                                          are recv_sf[e * sf_expert_stride + i *
                                          sf_token_stride + j * sf_hidden_stride]; else 0 */
+  int32_t layout_kernels;             /* kernels this layout launched: 1 (small problems, one
+                                         thread-block cluster) or 2 (count + assign) */
+  int32_t reserved1;
 } ep_layout_info;
 
 typedef struct ep_handle ep_handle;
@@ -208,6 +211,39 @@ EP_API ep_status ep_layout(const ep_config *cfg, const void *topk_idx, ep_stream
 EP_API ep_status ep_dispatch(ep_handle *h, const void *x, const float *topk_weights,
                       void *recv_x, float *recv_sf, float *recv_topk_weights,
                       int32_t *recv_topk_idx, ep_stream_t stream);
+
+/*
+ * ep_plan_layout -- the sizes ep_layout would report for a configuration
+ * with do_cpu_sync = 0 (they do not depend on the routing): rows_alloc (the
+ * upper bound), sf_numel, sf_token_stride, sf_hidden_stride, meta_rows,
+ * expert_capacity and sf_expert_stride.  Every pointer of *info is set to
+ * NULL and the counts to -1.  No GPU work.  EP_ERR_INVALID_ARG for
+ * do_cpu_sync = 1 or a NULL info.
+ */
+EP_API ep_status ep_plan_layout(const ep_config *cfg, ep_layout_info *info);
+
+/*
+ * ep_layout_dispatch -- ep_layout followed by ep_dispatch, in one call that
+ * takes the routing and the activations together, as the DeepEP README's
+ * low_latency_dispatch does ("Interfaces and examples").  Results are those
+ * of ep_layout and then ep_dispatch with the same arguments: the handle,
+ * *info (num_recv_tokens and num_expanded_tokens are -1) and the receive
+ * buffers.
+ *
+ * Requires do_cpu_sync = 0: the caller sizes the receive buffers from
+ * ep_plan_layout before the call.  topk_idx and x are read only during the
+ * call.  x, an input of the call, is complete before the layout starts, so
+ * the dispatch (launched right behind the layout kernels) loads and
+ * quantises the first source rows of every CTA while the layout runs; a
+ * separate ep_dispatch cannot, since the caller may write x in between.
+ * Errors as for ep_layout and ep_dispatch; on any error nothing is allocated
+ * and *out_handle is NULL.
+ */
+EP_API ep_status ep_layout_dispatch(const ep_config *cfg, const void *topk_idx, const void *x,
+                                    const float *topk_weights, void *recv_x, float *recv_sf,
+                                    float *recv_topk_weights, int32_t *recv_topk_idx,
+                                    ep_stream_t stream, ep_handle **out_handle,
+                                    ep_layout_info *info);
 
 /*
  * ep_dispatch_fp8 -- copy epilogue for an input that is already FP8 (§7.1:

@@ -65,7 +65,8 @@ int main(void) {
   P(ep_config, fixed_capacity) P(ep_config, reserved0)
   P(ep_layout_info, rows_alloc) P(ep_layout_info, topk_idx) P(ep_layout_info, error_word)
   P(ep_layout_info, meta_rows) P(ep_layout_info, expert_capacity)
-  P(ep_layout_info, sf_expert_stride) P(ep_layout_buffers, status)
+  P(ep_layout_info, sf_expert_stride) P(ep_layout_info, layout_kernels)
+  P(ep_layout_buffers, status)
   return 0;
 }
 '''
@@ -88,7 +89,7 @@ int main(void) {
               "num_sms", "cpu_sync_timeout_ms", "fixed_capacity", "reserved0"):
         assert got[("ep_config", f)] == getattr(C, f).offset, f
     for f in ("rows_alloc", "topk_idx", "error_word", "meta_rows", "expert_capacity",
-              "sf_expert_stride"):
+              "sf_expert_stride", "layout_kernels"):
         assert got[("ep_layout_info", f)] == getattr(I, f).offset, f
     assert got[("ep_layout_buffers", "status")] == B.status.offset
 
@@ -210,11 +211,67 @@ def test_entry_points_reject_bad_arguments_before_any_cuda_call(ep):
     T = 256 * 300
     big = ep.make_config(T, 8, 2048, 16, 128, T // 16 + 1, 1, True, False, False)
     assert fn(ctypes.byref(big), ctypes.c_void_p(0x1000), ctypes.byref(b), None) == 2
+    # layout + dispatch in one call: exact allocation, missing outputs, missing
+    # or misaligned x and receive buffers are refused on the host
+    ld = lib.ep_layout_dispatch
+    v = ctypes.c_void_p
+    nos = _cfg(ep, do_cpu_sync=False)  # BF16: recv_sf must be NULL
+
+    def call(cfg, x=v(0x1000), w=None, rx=v(0x1000), rsf=None, rw=None, out=True):
+        return ld(ctypes.byref(cfg), v(0x1000), x, w, rx, rsf, rw, None, None,
+                  ctypes.byref(h) if out else None, ctypes.byref(info))
+    assert call(_cfg(ep)) == 1                      # exact allocation (count wait)
+    assert call(nos, out=False) == 1                # no handle output
+    assert call(nos, x=None) == 1                   # missing x
+    assert call(nos, x=v(0x1008)) == 1              # x not 16-byte aligned
+    assert call(nos, rx=None) == 1                  # missing recv_x
+    assert call(nos, rsf=v(0x1000)) == 1            # scales for a BF16 dispatch
+    assert call(nos, rw=v(0x1000)) == 1             # weights out, none in
+    assert h.value is None
     # bounded-wait self-test: argument checks happen on the host
     st = lib.ep_selftest_bounded_wait
     st.argtypes = [ctypes.c_int32, ctypes.c_int32, ctypes.c_void_p, ctypes.c_void_p]
     assert st(1000, 0, None, None) == 1
     assert st(0, 0, ctypes.byref(ctypes.c_uint32()), None) == 1
+
+
+def test_plan_layout_sizes(ep):
+    """ep_plan_layout reports, without GPU work, the sizes ep.h states for a
+    layout without the count wait: the upper-bound rows and the scale-factor
+    layout of each mode."""
+    def al4(x):
+        return (x + 3) // 4 * 4
+    T, K, E, R, M, H = 300, 6, 32, 4, 80, 512
+    nb = H // 128
+    cases = [  # (expand, fp8, col_major, fixed)
+        (False, True, False, False), (False, True, True, False), (True, True, True, False),
+        (True, True, False, False), (False, False, False, False), (True, True, True, True),
+        (True, True, False, True), (True, False, False, True)]
+    for ex, fp8, cm, fixed in cases:
+        cfg = ep.make_config(T, K, E, R, H, M, 1 if fixed else 8, ex, False, False, fp8, cm,
+                             fixed_capacity=fixed)
+        info = ep.plan_layout(cfg)
+        rows = ep.upper_bound_rows(cfg)
+        cap = M * R if fixed else 0
+        assert info.rows_alloc == rows and info.meta_rows == rows
+        assert info.expert_capacity == cap
+        assert info.num_recv_tokens == -1 and info.num_expanded_tokens == -1
+        assert not info.dst_buffer_slot_idx and not info.error_word
+        if not fp8:
+            want = (0, 0, 0, 0)
+        elif fixed and cm:
+            want = (1, al4(cap), E * nb * al4(cap), nb * al4(cap))
+        elif fixed:
+            want = (nb, 1, E * nb * cap, nb * cap)
+        elif cm:
+            want = (1, al4(rows), nb * al4(rows), 0)
+        else:
+            want = (nb, 1, nb * rows, 0)
+        got = (info.sf_token_stride, info.sf_hidden_stride, info.sf_numel, info.sf_expert_stride)
+        assert got == want, (ex, fp8, cm, fixed)
+    with pytest.raises(ep.EpError):
+        ep.plan_layout(ep.make_config(T, K, E, R, H, M, 8, True, True, True))
+    assert ep.load_library().ep_plan_layout(ctypes.byref(_cfg(ep)), None) == 1
 
 
 def test_status_strings(ep):

@@ -40,18 +40,26 @@ def make_y(rows: int, H: int, seed: int, device) -> torch.Tensor:
 
 def run_and_check(ep, cfg, idx_cpu, x_cpu, w_cpu, *, y_seed=11, combine_tokens=None,
                   dispatch_tokens=None, with_weights=True, with_idx=True, combine_w=True,
-                  bias0=False, bias1=False, expert_bias=None):
+                  bias0=False, bias1=False, expert_bias=None, fused=False):
+    """Layout, dispatch and combine through the C ABI against the oracle.
+    fused: layout and dispatch by one ep_layout_dispatch call (no count
+    wait), into buffers sized by ep_plan_layout."""
     dev = torch.device("cuda")
     idx = idx_cpu.to(dev)
     x = x_cpu.to(dev)
     w = w_cpu.to(dev) if w_cpu is not None else None
-    h = ep.ep_layout(cfg, idx)
     lay = HN.oracle_layout(cfg, idx_cpu.to(torch.int64).numpy())
-    HN.check_layout(h, lay)
     use_fp8, cm = bool(cfg.use_fp8), bool(cfg.use_tma_aligned_col_major_sf)
-    out = ep.alloc_recv(h, with_weights=with_weights and w is not None,
-                        with_idx=with_idx and not cfg.do_expand)
-    ep.ep_dispatch(h, x, w, **out)
+    want_w, want_idx = with_weights and w is not None, with_idx and not cfg.do_expand
+    if fused:
+        out = ep.alloc_recv_planned(cfg, with_weights=want_w, with_idx=want_idx)
+        h = ep.ep_layout_dispatch(cfg, idx, x, w, **out)
+        HN.check_layout(h, lay)
+    else:
+        h = ep.ep_layout(cfg, idx)
+        HN.check_layout(h, lay)
+        out = ep.alloc_recv(h, with_weights=want_w, with_idx=want_idx)
+        ep.ep_dispatch(h, x, w, **out)
     x_bits = HN.bits16(x_cpu)
     w_np = None if w_cpu is None else w_cpu.numpy()
     if dispatch_tokens is None:
@@ -87,8 +95,9 @@ def run_and_check(ep, cfg, idx_cpu, x_cpu, w_cpu, *, y_seed=11, combine_tokens=N
                     else res)
     d = HN.ulp_diff(got, ref)
     assert d.max(initial=0) <= COMBINE_ULP, f"combine max ulp diff {d.max(initial=0)}"
+    kernels = int(h.info.layout_kernels)
     h.free()
-    return {"lay": lay, "combine_mismatch": int((d != 0).sum())}
+    return {"lay": lay, "combine_mismatch": int((d != 0).sum()), "layout_kernels": kernels}
 
 
 # ---------------------------------------------------------------------------
@@ -169,6 +178,19 @@ EDGE = {
     "many_src_ranks_small_m": (1000, 4, 32, 32, 64, 32, 2, True, True, True, False, False, 0.0, False),
     "max_topk": (64, 32, 64, 4, 128, 16, 4, True, True, True, True, True, 0.0, False),
     "many_experts": (256, 8, 2048, 16, 128, 16, 4, True, True, True, True, True, 0.0, False),
+    # Layouts of up to 16 chunks run as one thread-block cluster, larger ones
+    # as two kernels: both sides of the boundary, and a 9-CTA cluster with
+    # three ragged chunks per source rank.
+    "chunks_16_rank_nosync": (1024, 4, 32, 16, 128, 64, 1, False, False, False, True, False,
+                              0.05, False),
+    "chunks_16_expand_sync": (1000, 6, 64, 16, 256, 63, 8, True, True, True, True, True, 0.05,
+                              False),
+    "chunks_17_expand_sync": (1020, 6, 34, 17, 256, 60, 8, True, True, True, True, True, 0.05,
+                              False),
+    "chunks_17_rank_nosync": (1020, 4, 34, 17, 128, 60, 1, False, False, False, False, False,
+                              0.0, False),
+    "chunks_9_three_per_source": (1500, 8, 24, 3, 256, 700, 4, True, True, True, True, False,
+                                  0.1, True),
 }
 
 

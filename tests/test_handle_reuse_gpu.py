@@ -126,3 +126,29 @@ def test_independent_handles_on_two_streams(ep):
         d = HN.ulp_diff(HN.bits16(res[j]), ref)
         assert d.max(initial=0) <= 1
         handles[j].free()
+
+
+@pytest.mark.parametrize("expand", [False, True])
+def test_repeated_combines_on_one_handle(ep, expand):
+    """Back-to-back combines and dispatch_backward calls on one handle, with
+    the expert bias on and off: each gives what the oracle gives (nothing a
+    combine leaves behind changes the next one)."""
+    T, K, E, R, H, M = 3000, 6, 32, 4, 512, 750
+    idx, w = _routing(T, K, E, seed=41)
+    cfg = ep.make_config(T, K, E, R, H, M, 8 if expand else 1, expand, expand, True)
+    h = ep.ep_layout(cfg, idx.cuda())
+    lay = HN.oracle_layout(cfg, idx.numpy())
+    rows = h.rows_alloc
+    eb = W.hashed_bf16_rows(torch.arange(E), H, 77)
+    w_np = w.numpy()
+    for rep in range(3):
+        y = W.hashed_bf16_rows(torch.arange(rows), H, 50 + rep)
+        y_bits = HN.bits16(y)
+        use_eb = rep % 2 == 1
+        got = ep.ep_combine(h, y.cuda(), w.cuda(), None, None, eb.cuda() if use_eb else None)
+        ref = O.combine(lay, y_bits, w_np, None, None, HN.bits16(eb) if use_eb else None)
+        assert HN.ulp_diff(HN.bits16(got), ref).max(initial=0) == 0, rep
+        gx = ep.ep_dispatch_backward(h, y.cuda(), None)[0]
+        ref_b = O.combine(lay, y_bits, None, None, None, None)
+        assert HN.ulp_diff(HN.bits16(gx), ref_b).max(initial=0) == 0, rep
+    h.free()

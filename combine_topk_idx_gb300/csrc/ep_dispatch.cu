@@ -6,21 +6,24 @@
 // payload is e4m3 with one fp32 scale per 1x128 block (scale = amax / 448).
 //
 // Token-major scatter with persistent, warp-specialised CTAs:
-//   warp 0 (producer) takes tokens -- the CTA's index first, then the next
-//     free one from a handle counter -- issues one cp.async.bulk
-//     global->shared copy of the token's source row into a ring of input
-//     stages (3; 2 for quantised rows too large for three), then reads the
+//   warp 0 (producer) takes tokens -- CTA b's first S are b, b + G, ...
+//     (G CTAs, S stages), then the next free one from a handle counter --
+//     issues one cp.async.bulk global->shared copy of the token's source row
+//     into a ring of input stages (S = 3; 2 for quantised rows too large for
+//     three; the stage's "full" barrier counts the bytes), then reads the
 //     token's K destination rows (fetched while the previous token was
 //     issued), keeps the distinct ones (rank-layout slots of one rank share a
-//     row) and writes the per-row weights and local expert ids;
-//   the consumer warps wait for a stage and
+//     row), writes the per-row weights and local expert ids and arrives on
+//     the stage's "rows" barrier;
+//   the consumer warps wait for a stage's "full" barrier and
 //     FP8:  quantise it -- amax of each 128-element block by a 16-lane
 //           shuffle, scale = amax / 448 (IEEE division) and the e4m3 bytes of
 //           x / scale (packed cvt.rn.satfinite.e4m3x2 of a bracket of the
 //           quotient, IEEE quotients wherever the bracket straddles a
-//           rounding boundary) -- into an output stage, then one
-//           thread issues one cp.async.bulk shared->global store per distinct
-//           destination row while the others write the scales;
+//           rounding boundary) -- into an output stage, then, once "rows"
+//           completes, one thread issues one cp.async.bulk shared->global
+//           store per distinct destination row while the others write the
+//           scales;
 //     BF16: one thread stores the input stage itself to every row;
 //     pre-quantised FP8 input (x given as e4m3 bytes + fp32 scales, §7.1):
 //           the same copy of the H-byte row, while the other threads copy
@@ -29,8 +32,12 @@
 // The source row is read from HBM once and quantised once whatever K is; the
 // TMA engine moves every payload byte.  After the tokens, the consumer warps
 // zero the alignment padding rows in 8-row work items, also handed out from a
-// handle counter.  Every mbarrier wait
-// is bounded: a wait that gives up sets EP_ERRBIT_TIMEOUT and the CTA returns.
+// handle counter.  The kernel is launched with programmatic dependent
+// launch: nothing reads the layout's outputs before griddepcontrol.wait; with
+// early_x (the layout was launched by the same call, so x was complete before
+// it) the first S source rows are loaded, and quantised, before the wait.
+// Every mbarrier wait is bounded: a wait that gives up sets EP_ERRBIT_TIMEOUT
+// and the CTA returns.
 #include <algorithm>
 
 #include "ep_internal.cuh"

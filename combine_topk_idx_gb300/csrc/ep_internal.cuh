@@ -12,9 +12,10 @@ constexpr int kFp8Block = 128;          // 1x128 scale blocks
 constexpr int kLayoutThreads = 1024;     // assign kernel CTA
 constexpr int kLayoutChunkTokens = 256;  // tokens per layout chunk (<= 8192 slots with K <= 32)
 // Rank layouts of at most this many chunks run as one kernel whose grid is a
-// single thread-block cluster (above 8 CTAs: a non-portable cluster size), if
-// its shared memory fits kLayoutClusterSmem and the device can place it.
-constexpr int kLayoutClusterChunks = 16;
+// single thread-block cluster of one CTA per chunk plus one (above 8 CTAs: a
+// non-portable cluster size, at most 16), if its shared memory fits
+// kLayoutClusterSmem and the device can place it.
+constexpr int kLayoutClusterChunks = 15;
 constexpr size_t kLayoutClusterSmem = 96 * 1024;
 
 // Control words at the head of the handle's device block.

@@ -342,35 +342,34 @@ __device__ __forceinline__ void column_sums(int nk, int nb, int b, ColumnOf colu
   }
 }
 
-// ---------------- cluster form ----------------
+// ---------------- cluster form (rank layout) ----------------
 
 size_t cluster_head_ints(const LayoutParams &p) {
-  return 6 * (size_t)p.E + 4 * (size_t)p.R + 2 + 2 * (size_t)p.chunk_tokens * p.K;
+  return 6 * (size_t)p.E + 4 * (size_t)p.R + 2 + (size_t)p.chunk_tokens * p.K * 2;
 }
 
+// CTAs 0..nb-1 own the chunks; CTA nb, the last of the cluster, owns none and
+// writes the global counts and prefix sums.
 __global__ void __launch_bounds__(NT, 1) layout_cluster_kernel(LayoutParams p) {
   extern __shared__ __align__(16) int smem[];
   const int K = p.K, L = p.L, R = p.R, E = p.E, A = p.A;
-  const bool expand = p.do_expand != 0;
-  const int nkey = expand ? E : R;
   const int cap = p.chunk_tokens * K;
-  const int nb = p.num_blocks;  // the grid is one cluster: CTA rank = blockIdx.x
-  const int fcap = p.fixed_cap;
+  const int nb = p.num_blocks;  // chunks; the grid is one cluster of nb + 1 CTAs
   const int nrw = p.rank_warps;
   // Read by the other CTAs of the cluster: this chunk's expert counts, rank
   // counts and error bits.
   int *pub = smem;                     // [E + R + 1]
   int *rank_of = pub + E + R + 1;      // [E] owning rank of each expert
   int *idx_s = rank_of + E;            // [cap]
-  // [cap] per slot: its key, then its rank among the chunk's slots of the
-  // key; -1 for an empty slot; rank layout: -(j + 2) for a slot whose row is
-  // owned by the token's lower slot j (chunk-relative) on the same rank
+  // [cap] per slot: the rank for the token's lowest slot on that rank (then
+  // its rank among the chunk's such slots); -1 for an empty slot; -(j + 2)
+  // for a slot whose row the token's lower slot j (chunk-relative) owns
   int *loc_s = idx_s + cap;
   int *tot_s = loc_s + cap;            // [E + R] totals over all chunks
   int *bef_s = tot_s + E + R;          // [E + R] totals of the chunks before this one
   int *scan_s = bef_s + E + R;         // [2E + R + 1]
   const int head = 6 * E + 4 * R + 2 + 2 * cap;
-  // [nkey][nrw + 1] key words of the ranking ranges: key-major, so a warp
+  // [R][nrw + 1] key words of the ranking ranges: key-major, so a warp
   // scans a key's ranges without bank conflicts; the odd row length spreads
   // the keys of one range (the atomics of the slot pass and the ranking)
   // over the banks
@@ -379,8 +378,9 @@ __global__ void __launch_bounds__(NT, 1) layout_cluster_kernel(LayoutParams p) {
   __shared__ int warp_tot[NWARPS + 1];
 
   const int b = blockIdx.x;
-  int t0;
-  const int nt = chunk_of(p, b, t0);
+  const bool outputs_cta = b == nb;
+  int t0 = p.T, nt = 0;
+  if (!outputs_cta) nt = chunk_of(p, b, t0);
   const int ns = nt * K;
   const int64_t base = (int64_t)t0 * K;
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
@@ -399,7 +399,7 @@ __global__ void __launch_bounds__(NT, 1) layout_cluster_kernel(LayoutParams p) {
   }
   for (int i = threadIdx.x; i < E + R + 1; i += NT) pub[i] = 0;
   for (int e = threadIdx.x; e < E; e += NT) rank_of[e] = e / L;
-  for (int i = threadIdx.x; i < kw * nkey; i += NT) whist[i] = 0ull;
+  for (int i = threadIdx.x; i < kw * R; i += NT) whist[i] = 0ull;
   uint8_t *in_rank = p.in_rank + (int64_t)t0 * R;
   if ((R & 3) == 0)
     for (int i = threadIdx.x; i < nt * R / 4; i += NT) reinterpret_cast<uint32_t *>(in_rank)[i] = 0;
@@ -426,20 +426,19 @@ __global__ void __launch_bounds__(NT, 1) layout_cluster_kernel(LayoutParams p) {
   if (lane == 0 && err) atomicOr(reinterpret_cast<unsigned *>(&pub[E + R]), err);
   __syncthreads();
 
-  // One thread per slot (warp-uniform trips, for the ballots): the token's
-  // rank set, the slot's key and its count in its ranking range; warp w < nrw
-  // ranks the slots [w * per, (w + 1) * per).  The chunk's counts of the keys
-  // come from the ranges below; the other counts (experts in the rank layout,
-  // ranks in the expanded layouts) are added here.
+  // One thread per slot: the token's lowest slot on each rank (a look-back
+  // over the token's slots) sets its is_token_in_rank byte and is the rank's
+  // key, counted in its ranking range (warp w < nrw ranks the slots
+  // [w * per, (w + 1) * per)); the expert counts by shared atomics.  The
+  // chunk's rank counts are the key totals, from the range bases below.
   const int per = max(1, (ns + nrw - 1) / nrw);
-  for (int i0 = warp * 32; i0 < ns; i0 += NT) {
-    const int i = i0 + lane;
-    const int e = i < ns ? idx_s[i] : -1;
-    int key = -1, r = -1;
+  for (int i = threadIdx.x; i < ns; i += NT) {
+    const int e = idx_s[i];
+    int key = -1;
     if (e >= 0) {
       const int t = i / K, j0 = t * K;
-      r = rank_of[e];
-      int own = i;  // the token's lowest slot on rank r
+      const int r = rank_of[e];
+      int own = i;
       for (int j = j0; j < i; ++j) {
         const int f = idx_s[j];
         if (f >= 0 && rank_of[f] == r) {
@@ -447,44 +446,31 @@ __global__ void __launch_bounds__(NT, 1) layout_cluster_kernel(LayoutParams p) {
           break;
         }
       }
-      if (own == i)
+      atomicAdd(&pub[e], 1);
+      if (own == i) {
         in_rank[t * R + r] = 1;
-      if (!expand) atomicAdd(&pub[e], 1);
-      key = expand ? e : own == i ? r : -(own + 2);
-      if (key >= 0)
-        atomicAdd(reinterpret_cast<unsigned *>(&whist[(size_t)key * kw + i / per]), 1u);
-      if (own != i) r = -1;  // r now marks the token's first slot on the rank
-    }
-    if (i < ns) loc_s[i] = key;
-    if (expand) {
-      if (R <= 32) {
-        const unsigned firsts = __ballot_sync(0xffffffffu, r >= 0);
-        for (int rr = 0; rr < R && firsts; ++rr) {
-          const int c = __popc(__ballot_sync(0xffffffffu, r == rr));
-          if (lane == 0 && c) atomicAdd(&pub[E + rr], c);
-        }
-      } else if (r >= 0) {
-        atomicAdd(&pub[E + r], 1);
+        key = r;
+        atomicAdd(reinterpret_cast<unsigned *>(&whist[(size_t)r * kw + i / per]), 1u);
+      } else {
+        key = -(own + 2);
       }
     }
+    loc_s[i] = key;
   }
   __syncthreads();
-  // Each range's start per key (warp per key, lanes = ranges); the key's
+  // Each range's start per rank (warp per rank, lanes = ranges); the rank's
   // total is the chunk's count of it.
-  {
-    const int koff = expand ? 0 : E;
-    for (int key = warp; key < nkey; key += NWARPS) {
-      unsigned long long *wk = whist + (size_t)key * kw;
-      const unsigned c = lane < nrw ? (unsigned)wk[lane] : 0u;
-      unsigned incl = c;
+  for (int r = warp; r < R; r += NWARPS) {
+    unsigned long long *wk = whist + (size_t)r * kw;
+    const unsigned c = lane < nrw ? (unsigned)wk[lane] : 0u;
+    unsigned incl = c;
 #pragma unroll
-      for (int o = 1; o < 32; o <<= 1) {
-        const unsigned y = __shfl_up_sync(0xffffffffu, incl, o);
-        if (lane >= o) incl += y;
-      }
-      if (lane < nrw) wk[lane] = incl - c;
-      if (lane == 31) pub[koff + key] = (int)incl;
+    for (int o = 1; o < 32; o <<= 1) {
+      const unsigned y = __shfl_up_sync(0xffffffffu, incl, o);
+      if (lane >= o) incl += y;
     }
+    if (lane < nrw) wk[lane] = incl - c;
+    if (lane == 31) pub[E + r] = (int)incl;
   }
   __syncthreads();
   cluster_arrive_release();  // this chunk's counts are published
@@ -498,61 +484,70 @@ __global__ void __launch_bounds__(NT, 1) layout_cluster_kernel(LayoutParams p) {
   __syncwarp();    // the cluster barriers are .aligned: whole warps
   cluster_wait();  // every chunk's counts are published
 
-  // Column sums over the cluster's chunks: totals and the chunks before this.
-  column_sums<NT>(
-      E + R, nb, b,
-      [&](int key) {
-        const uint32_t a = smem_u32(pub + key);
-        return [a](int c) { return ld_cluster_s32(a, (uint32_t)c); };
-      },
-      tot_s, bef_s);
-  unsigned err_all = 0;
-  if (b == 0 && warp == 0)
-    for (int c = lane; c < nb; c += 32) err_all |= (unsigned)ld_cluster_s32(smem_u32(pub + E + R), c);
-  __syncwarp();
-  cluster_arrive_relaxed();  // done reading the other CTAs' shared memory
-  __syncthreads();
-
-  cta_exclusive_scan<NT>(
-      2 * E + R,
-      [&](int i) {
-        return i < E ? tot_s[i] : i < 2 * E ? (tot_s[i - E] + A - 1) / A * A : tot_s[i - E];
-      },
-      scan_s, warp_tot);
-  write_psum_rs<NT>(p, b, bef_s + E, tot_s + E, b == 0);
-  if (b == 0) write_outputs<NT>(p, tot_s, scan_s, err_all);
-
-  // Segment starts of the sort key: the fixed per-expert capacity, the
-  // aligned expert counts, or the rank counts.
-  const int a0 = scan_s[E], r0 = scan_s[2 * E];
-  auto seg = [&](int key) {
-    return fcap > 0 ? key * fcap : expand ? scan_s[E + key] - a0 : scan_s[2 * E + key] - r0;
-  };
-  const int boff = expand ? 0 : E;
-  int2 *meta = reinterpret_cast<int2 *>(p.meta);
-  for (int i = threadIdx.x; i < ns; i += NT) {
-    const int e = idx_s[i];
-    const int loc = loc_s[i];
-    int row = -1;
-    if (loc >= 0) {
-      const int key = expand ? e : rank_of[e];
-      row = seg(key) + bef_s[boff + key] + loc;
-      bool keep = row < p.row_limit;
-      if (fcap > 0 && row >= (key + 1) * fcap) keep = false;  // past capacity
-      if (keep) {
-        const int t = i / K;
-        meta[row] = make_int2(t0 + t, i - t * K);
-      } else {
-        row = -1;
+  if (outputs_cta) {
+    // Column sums of every count over the chunks, one CTA-wide scan of
+    // [counts | aligned counts | rank counts], the global outputs.
+    column_sums<NT>(
+        E + R, nb, b,
+        [&](int key) {
+          const uint32_t a = smem_u32(pub + key);
+          return [a](int c) { return ld_cluster_s32(a, (uint32_t)c); };
+        },
+        tot_s, bef_s);
+    unsigned err_all = 0;
+    if (warp == 0)
+      for (int c = lane; c < nb; c += 32)
+        err_all |= (unsigned)ld_cluster_s32(smem_u32(pub + E + R), c);
+    __syncwarp();
+    cluster_arrive_relaxed();  // done reading the other CTAs' shared memory
+    __syncthreads();
+    cta_exclusive_scan<NT>(
+        2 * E + R,
+        [&](int i) {
+          return i < E ? tot_s[i] : i < 2 * E ? (tot_s[i - E] + A - 1) / A * A : tot_s[i - E];
+        },
+        scan_s, warp_tot);
+    write_psum_rs<NT>(p, b, bef_s + E, tot_s + E, true);
+    write_outputs<NT>(p, tot_s, scan_s, err_all);
+  } else {
+    // The rank counts only: totals and the chunks before this one, then the
+    // rank segment starts.
+    column_sums<NT>(
+        R, nb, b,
+        [&](int key) {
+          const uint32_t a = smem_u32(pub + E + key);
+          return [a](int c) { return ld_cluster_s32(a, (uint32_t)c); };
+        },
+        tot_s + E, bef_s + E);
+    __syncwarp();
+    cluster_arrive_relaxed();  // done reading the other CTAs' shared memory
+    __syncthreads();
+    cta_exclusive_scan<NT>(R, [&](int r) { return tot_s[E + r]; }, scan_s, warp_tot);
+    write_psum_rs<NT>(p, b, bef_s + E, tot_s + E, false);
+    // Rows: segment start + the chunks before + the rank among the chunk's
+    // slots; a slot whose row a lower slot of the token owns takes that row.
+    int2 *meta = reinterpret_cast<int2 *>(p.meta);
+    for (int i = threadIdx.x; i < ns; i += NT) {
+      const int e = idx_s[i];
+      const int loc = loc_s[i];
+      int row = -1;
+      if (loc >= 0) {
+        const int r = rank_of[e];
+        row = scan_s[r] + bef_s[E + r] + loc;
+        if (row < p.row_limit) {
+          const int t = i / K;
+          meta[row] = make_int2(t0 + t, i - t * K);
+        } else {
+          row = -1;
+        }
+      } else if (loc <= -2) {
+        const int r = rank_of[e];
+        row = scan_s[r] + bef_s[E + r] + loc_s[-loc - 2];
+        if (row >= p.row_limit) row = -1;
       }
-    } else if (loc <= -2) {  // rank layout: the owner slot's row
-      const int r = rank_of[e];
-      row = seg(r) + bef_s[E + r] + loc_s[-loc - 2];
-      if (row >= p.row_limit) row = -1;
+      p.dst[base + i] = row;
     }
-    p.dst[base + i] = row;
   }
-  if (expand && fcap == 0) write_padding<NT>(p, b, nb, tot_s, seg);
   __syncwarp();
   cluster_wait();  // no CTA leaves while another may still read its counts
 }
@@ -744,10 +739,9 @@ __global__ void __launch_bounds__(NT, 1) layout_assign_kernel(LayoutParams p) {
 }
 
 size_t cluster_smem(const LayoutParams &p) {
-  const int nkey = p.do_expand ? p.E : p.R;
   const size_t head = cluster_head_ints(p);
   return sizeof(int) * (head + (head & 1)) +
-         sizeof(unsigned long long) * (size_t)(p.rank_warps + 1) * nkey;
+         sizeof(unsigned long long) * (size_t)(p.rank_warps + 1) * p.R;
 }
 
 // Whether a cluster of `nb` CTAs of the cluster kernel at `smem` bytes can be
@@ -823,17 +817,17 @@ cudaError_t launch_layout(const LayoutParams &p, cudaStream_t s, int *kernels) {
   // layouts keep two kernels.
   if (!p.do_expand && p.num_blocks <= kLayoutClusterChunks && smem_cl <= kLayoutClusterSmem) {
     bool ok = false;
-    cudaError_t err = cluster_launchable(p.num_blocks, smem_cl, &ok);
+    cudaError_t err = cluster_launchable(p.num_blocks + 1, smem_cl, &ok);
     if (err != cudaSuccess) return err;
     if (ok) {
       cudaLaunchConfig_t lc{};
-      lc.gridDim = dim3(p.num_blocks);
+      lc.gridDim = dim3(p.num_blocks + 1);  // + the outputs CTA
       lc.blockDim = dim3(NT);
       lc.dynamicSmemBytes = smem_cl;
       lc.stream = s;
       cudaLaunchAttribute attr[1];
       attr[0].id = cudaLaunchAttributeClusterDimension;
-      attr[0].val.clusterDim.x = p.num_blocks;
+      attr[0].val.clusterDim.x = p.num_blocks + 1;
       attr[0].val.clusterDim.y = 1;
       attr[0].val.clusterDim.z = 1;
       lc.attrs = attr;

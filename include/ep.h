@@ -147,8 +147,9 @@ typedef struct ep_layout_info {
   int64_t sf_expert_stride;           /* fixed_capacity: the scales of row e * capacity + i
                                          are recv_sf[e * sf_expert_stride + i *
                                          sf_token_stride + j * sf_hidden_stride]; else 0 */
-  int32_t layout_kernels;             /* kernels this layout launched: 1 (small problems, one
-                                         thread-block cluster) or 2 (count + assign) */
+  int32_t layout_kernels;             /* kernels this layout launched: 1 (rank layouts of at
+                                         most 16 chunks of 256 tokens: one thread-block
+                                         cluster) or 2 (count + assign) */
   int32_t reserved1;
 } ep_layout_info;
 

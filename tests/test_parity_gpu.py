@@ -178,9 +178,12 @@ EDGE = {
     "many_src_ranks_small_m": (1000, 4, 32, 32, 64, 32, 2, True, True, True, False, False, 0.0, False),
     "max_topk": (64, 32, 64, 4, 128, 16, 4, True, True, True, True, True, 0.0, False),
     "many_experts": (256, 8, 2048, 16, 128, 16, 4, True, True, True, True, True, 0.0, False),
-    # Layouts of up to 16 chunks run as one thread-block cluster, larger ones
-    # as two kernels: both sides of the boundary, and a 9-CTA cluster with
-    # three ragged chunks per source rank.
+    # Rank layouts of up to 15 chunks run as one thread-block cluster (a CTA
+    # per chunk and one more), larger ones and the expanded layouts as two
+    # kernels: both sides of the boundary, and three ragged chunks per source
+    # rank.
+    "chunks_15_rank_sync": (960, 5, 48, 16, 256, 64, 1, False, False, True, True, False, 0.05,
+                            False),
     "chunks_16_rank_nosync": (1024, 4, 32, 16, 128, 64, 1, False, False, False, True, False,
                               0.05, False),
     "chunks_16_expand_sync": (1000, 6, 64, 16, 256, 63, 8, True, True, True, True, True, 0.05,
@@ -385,11 +388,14 @@ def test_layout_deterministic_and_cached_dispatch(ep):
 
 
 @pytest.mark.parametrize("name,T", [("decode", None), ("large", 2048)])
-def test_cuda_graph_capture_and_replay(ep, name, T):
+@pytest.mark.parametrize("one_call", [False, True])
+def test_cuda_graph_capture_and_replay(ep, name, T, one_call):
     """Without the host count wait the whole path is stream-ordered: capture
     layout + dispatch + combine (+ handle free) in a CUDA graph, replay it on
     new inputs copied into the captured buffers, and compare with an eager
-    run of the same inputs."""
+    run of the same inputs.  one_call: layout and dispatch captured as one
+    ep_layout_dispatch call (its early source-row loads ride on the
+    programmatic-dependent-launch edge of the graph)."""
     wl = W.WORKLOADS[name]
     T = wl.num_tokens if T is None else T
     cfg = HN.cfg_for(ep, wl, T=T, do_cpu_sync=False)
@@ -416,8 +422,11 @@ def test_cuda_graph_capture_and_replay(ep, name, T):
         x_s.copy_(inp["x"])
 
     def path(st):
-        h = ep.ep_layout(cfg, idx_s, stream=st)
-        ep.ep_dispatch(h, x_s, w_s, stream=st, **recv)
+        if one_call:
+            h = ep.ep_layout_dispatch(cfg, idx_s, x_s, w_s, stream=st, **recv)
+        else:
+            h = ep.ep_layout(cfg, idx_s, stream=st)
+            ep.ep_dispatch(h, x_s, w_s, stream=st, **recv)
         ep.ep_combine(h, y_s, w_s, out=res, stream=st)
         h.free()
 

@@ -29,7 +29,7 @@ EP_ERR_OVERFLOW = 7
 EP_ERRBIT_BAD_TOPK_IDX = 1
 EP_ERRBIT_OVERFLOW = 2
 EP_ERRBIT_TIMEOUT = 4
-EP_ABI_VERSION = 2
+EP_ABI_VERSION = 3
 
 
 class EpError(RuntimeError):

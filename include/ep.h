@@ -435,7 +435,7 @@ EP_API ep_status ep_upper_bound_rows(const ep_config *cfg, int64_t *rows);
 EP_API ep_status ep_host_wait_flag(const volatile int32_t *flag, int32_t expected,
                             int32_t timeout_ms);
 
-#define EP_ABI_VERSION 2
+#define EP_ABI_VERSION 3
 
 #ifdef __cplusplus
 }

@@ -197,6 +197,18 @@ EDGE = {
 }
 
 
+# Layout form the boundary cases must take: 1 = the cluster kernel, 2 = the
+# count and assign kernels.
+EDGE_FORM = {
+    "chunks_15_rank_sync": 1,
+    "chunks_16_rank_nosync": 2,
+    "chunks_16_expand_sync": 2,
+    "chunks_17_expand_sync": 2,
+    "chunks_17_rank_nosync": 2,
+    "chunks_9_three_per_source": 2,
+}
+
+
 @pytest.mark.parametrize("case", sorted(EDGE))
 def test_edge_cases(ep, case):
     T, K, E, R, H, M, A, ex, zp, sync, fp8, cm, drop, dup = EDGE[case]
@@ -204,7 +216,9 @@ def test_edge_cases(ep, case):
     g = torch.Generator().manual_seed(3)
     x = torch.randn(T, H, generator=g).to(torch.bfloat16)
     cfg = ep.make_config(T, K, E, R, H, M, A, ex, zp, sync, fp8, cm)
-    run_and_check(ep, cfg, idx, x, w, bias0=True)
+    r = run_and_check(ep, cfg, idx, x, w, bias0=True)
+    if case in EDGE_FORM:
+        assert r["layout_kernels"] == EDGE_FORM[case]
 
 
 def test_combine_variants(ep):

@@ -166,7 +166,7 @@ __device__ __forceinline__ void reduce_vectors(const CombineParams &p, const Sta
   }
 }
 
-template <bool HAS_W, bool HAS_EB, int NV>
+template <bool HAS_W, bool HAS_EB, int NV, bool STEP>
 __global__ void __launch_bounds__(kMaxConsumers + 32, 1)
     combine_kernel(CombineParams p, int chunk_bytes, int nchunks, int slots_cap) {
   extern __shared__ __align__(128) uint8_t smem[];
@@ -177,10 +177,8 @@ __global__ void __launch_bounds__(kMaxConsumers + 32, 1)
   const int H = p.H;
   const int64_t row_bytes = 2 * (int64_t)H;
   const int64_t stage_bytes = (int64_t)slots_cap * chunk_bytes;
-  // The expert-bias combine is bound by instruction issue, so it steps its
-  // units without divisions.  The others keep the division: stepping there
-  // measured 2-3 us slower on the HBM-bound 4096 x 7168 top-8 combine.
-  using Cursor = UnitCursor<HAS_EB>;
+  // STEP: units stepped with adds only (the launcher's choice).
+  using Cursor = UnitCursor<STEP>;
   const int64_t G = gridDim.x;
   const int gq = (int)(G / nchunks), gr = (int)(G % nchunks);
   const int has_b0 = p.bias0 != nullptr, has_b1 = p.bias1 != nullptr;
@@ -303,9 +301,11 @@ __global__ void __launch_bounds__(kMaxConsumers + 32, 1)
   }
 }
 
+// Units per CTA up to which the units are stepped with adds only.
+constexpr int64_t kStepUnitsPerCta = 16;
+
 template <bool W, bool EB, int NV>
 cudaError_t launch_one(const CombineParams &p, int sm_cap, cudaStream_t s) {
-  auto kern = combine_kernel<W, EB, NV>;
   const int64_t row_bytes = 2 * (int64_t)p.H;
   const int nbias = (p.bias0 != nullptr) + (p.bias1 != nullptr);
   const int slots_cap = p.K + nbias;
@@ -325,15 +325,31 @@ cudaError_t launch_one(const CombineParams &p, int sm_cap, cudaStream_t s) {
   const int consumers = std::min(kMaxConsumers, ((nv + NV - 1) / NV + 31) / 32 * 32);
   const int threads = consumers + 32;
   const size_t smem = (size_t)kStages * slots_cap * chunk;
+  const int64_t units = (int64_t)p.T * nchunks;
+  // Unit cursor: adds only for the expert-bias combine (bound by instruction
+  // issue: skewed 162 -> 152 us) and for short combines, where each CTA's
+  // 64-bit divisions lie on its latency path (decode 23.3 -> 21.1 us, step
+  // 39.9 -> 38.0 us); the long HBM-bound combines measured faster with the
+  // division (prefill 78.3 -> 76.2 us, 32768 tokens 635 -> 624 us).  The
+  // grid, and so the choice, comes from the stepping kernel's occupancy; the
+  // division kernel has its own shared-memory opt-in and occupancy.
+  auto kern = combine_kernel<W, EB, NV, true>;
+  const void *func = reinterpret_cast<const void *>(kern);
   int dev = 0, per_sm = 0;
-  cudaError_t err =
-      launch_geometry(reinterpret_cast<const void *>(kern), threads, smem, &dev, &per_sm);
+  cudaError_t err = launch_geometry(func, threads, smem, &dev, &per_sm);
   if (err != cudaSuccess) return err;
-  if (per_sm < 1) per_sm = 1;
   const int sms = device_sm_count(dev);
   const int use_sms = (sm_cap > 0 && sm_cap < sms) ? sm_cap : sms;
-  const int64_t units = (int64_t)p.T * nchunks;
-  const int64_t grid = std::min<int64_t>((int64_t)use_sms * per_sm, units);
+  int64_t grid = std::min<int64_t>((int64_t)use_sms * std::max(per_sm, 1), units);
+  if constexpr (!EB) {
+    if (units > kStepUnitsPerCta * grid) {
+      kern = combine_kernel<W, EB, NV, false>;
+      func = reinterpret_cast<const void *>(kern);
+      err = launch_geometry(func, threads, smem, &dev, &per_sm);
+      if (err != cudaSuccess) return err;
+      grid = std::min<int64_t>((int64_t)use_sms * std::max(per_sm, 1), units);
+    }
+  }
   if (grid <= 0) return cudaSuccess;
   // programmatic dependent launch: the prologue overlaps the previous kernel
   cudaLaunchConfig_t lc{};

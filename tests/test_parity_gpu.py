@@ -528,6 +528,26 @@ def test_maximum_hidden_backward_pair(ep):
     check_backward(ep, ep.make_config(T, K, E, R, H, M, 8, True, True, False, False, False), idx)
 
 
+def test_short_combine_grid_strides(ep):
+    """Short combines (at most 16 units per CTA) step each CTA's (token,
+    chunk) by the grid stride with adds only, also without a per-expert bias.
+    Hidden 7168 splits into 4 chunks; grids of 2, 6 and 10 CTAs (1, 3 and 5
+    SMs) over 7 to 37 tokens give strides that wrap a row end and up to 16
+    units per CTA, and 64 tokens on the full grid one unit per CTA.
+    Weighted with a per-token bias, and unweighted; both layouts; every
+    output against the oracle."""
+    K, E, R, H = 8, 32, 4, 7168
+    for T, sms in ((7, 1), (23, 3), (37, 5), (64, 0)):
+        M = (T + R - 1) // R
+        idx, w = _routing(T, K, E, seed=40 + T, drop=0.05)
+        x = torch.randn(T, H, generator=torch.Generator().manual_seed(T)).to(torch.bfloat16)
+        for expand in (False, True):
+            cfg = ep.make_config(T, K, E, R, H, M, 4 if expand else 1, expand, expand, True,
+                                 num_sms=sms)
+            run_and_check(ep, cfg, idx, x, w, bias0=True)
+            run_and_check(ep, cfg, idx, x, w, combine_w=False)
+
+
 @pytest.mark.parametrize("expand", [False, True])
 def test_expert_bias_combine_grid_strides(ep, expand):
     """The per-expert-bias combine steps each CTA's (token, chunk) by the grid

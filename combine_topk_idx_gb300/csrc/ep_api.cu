@@ -449,6 +449,7 @@ ep_status layout_setup(const ep_config *cfg, const void *topk_idx, ep_stream_t s
   const int64_t nblocks = std::max<int64_t>(1, src_ranks * lp.blocks_per_src);
   if (nblocks > 0x7fffffff) return EP_ERR_UNSUPPORTED;
   lp.num_blocks = (int)nblocks;
+  lp.src_ranks = (int)src_ranks;
   lp.rank_warps = layout_rank_warps(c.do_expand ? E : R);
   if (layout_assign_smem(lp) > 220 * 1024) return EP_ERR_UNSUPPORTED;
 

@@ -48,6 +48,7 @@ struct LayoutParams {
                           // by the layout
   int num_blocks;         // layout grid (one CTA per chunk of tokens)
   int blocks_per_src;     // chunks per source rank
+  int src_ranks;          // source ranks holding tokens: ceil(T / M)
   int chunk_tokens;       // tokens per chunk
   int rank_warps;         // warps that rank slots in the assign kernel
   int64_t row_limit;      // rows at or past this are dropped (overflow)

@@ -226,7 +226,7 @@ template <int kThreads>
 __device__ __forceinline__ void write_psum_rs(const LayoutParams &p, int b, const int *bef_r,
                                               const int *tot_r, bool empty_sources) {
   const int R = p.R, RR = R + 1;
-  const int src_real = p.T > 0 ? (int)(((int64_t)p.T + p.M - 1) / p.M) : 0;
+  const int src_real = p.src_ranks;
   const int s = b / p.blocks_per_src;
   if (b < p.num_blocks && b == s * p.blocks_per_src && s < src_real)
     for (int r = threadIdx.x; r < R; r += kThreads) p.psum_rs[(int64_t)r * RR + s] = bef_r[r];
@@ -244,14 +244,14 @@ __device__ __forceinline__ void write_psum_rs(const LayoutParams &p, int b, cons
 template <int kThreads>
 __device__ __forceinline__ void write_outputs(const LayoutParams &p, const int *tot_s,
                                               const int32_t *scan_s, unsigned err) {
-  const int E = p.E, R = p.R, A = p.A, fcap = p.fixed_cap;
+  const int E = p.E, R = p.R, fcap = p.fixed_cap;
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
   const int a0 = scan_s[E], r0 = scan_s[2 * E];
   for (int e = threadIdx.x; e <= E; e += kThreads) {
     const int pc = scan_s[e], pa = scan_s[E + e] - a0;
     if (e < E) {
       p.cnt_e[e] = tot_s[e];
-      p.cnt_e_al[e] = (tot_s[e] + A - 1) / A * A;
+      p.cnt_e_al[e] = scan_s[E + e + 1] - scan_s[E + e];  // aligned count
     }
     p.psum_e[e] = fcap > 0 ? pc : pa;  // fixed capacity: the prefix of the counts
     p.psum_pad[e] = pa - pc;

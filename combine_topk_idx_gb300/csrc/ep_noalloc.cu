@@ -80,6 +80,7 @@ extern "C" ep_status ep_layout_noalloc(const ep_config *cfg, const void *topk_id
   const int64_t max_tok = std::min<int64_t>(lp.M, T);
   lp.blocks_per_src = (int)std::max<int64_t>(1, (max_tok + lp.chunk_tokens - 1) / lp.chunk_tokens);
   const int64_t chunks = std::max<int64_t>(1, src_ranks * lp.blocks_per_src);
+  lp.src_ranks = (int)src_ranks;
   const int64_t words = chunks * ((int64_t)E + R + 1);
   if (words > EP_NOALLOC_SCRATCH_WORDS) return EP_ERR_UNSUPPORTED;
   lp.num_blocks = (int)chunks;

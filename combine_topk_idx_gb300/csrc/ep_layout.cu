@@ -507,7 +507,6 @@ __global__ void __launch_bounds__(NT, 1) layout_cluster_kernel(LayoutParams p) {
           return i < E ? tot_s[i] : i < 2 * E ? (tot_s[i - E] + A - 1) / A * A : tot_s[i - E];
         },
         scan_s, warp_tot);
-    write_psum_rs<NT>(p, b, bef_s + E, tot_s + E, true);
     write_outputs<NT>(p, tot_s, scan_s, err_all);
   } else {
     // The rank counts only: totals and the chunks before this one, then the
@@ -523,7 +522,9 @@ __global__ void __launch_bounds__(NT, 1) layout_cluster_kernel(LayoutParams p) {
     cluster_arrive_relaxed();  // done reading the other CTAs' shared memory
     __syncthreads();
     cta_exclusive_scan<NT>(R, [&](int r) { return tot_s[E + r]; }, scan_s, warp_tot);
-    write_psum_rs<NT>(p, b, bef_s + E, tot_s + E, false);
+    // the last chunk's CTA also writes the columns of source ranks without
+    // tokens (from the rank totals), off the outputs CTA's path
+    write_psum_rs<NT>(p, b, bef_s + E, tot_s + E, b == nb - 1);
     // Rows: segment start + the chunks before + the rank among the chunk's
     // slots; a slot whose row a lower slot of the token owns takes that row.
     int2 *meta = reinterpret_cast<int2 *>(p.meta);
@@ -628,7 +629,7 @@ __global__ void __launch_bounds__(NT, 1) layout_assign_kernel(LayoutParams p) {
       },
       tot_s, bef_s);
   __syncthreads();
-  write_psum_rs<NT>(p, b, bef_s + E, tot_s + E, b == p.num_blocks);
+  write_psum_rs<NT>(p, b, bef_s + E, tot_s + E, b == p.num_blocks - 1);
 
   const int fcap = p.fixed_cap;
   if (b == p.num_blocks) {

@@ -194,6 +194,13 @@ EDGE = {
                               0.0, False),
     "chunks_9_three_per_source": (1500, 8, 24, 3, 256, 700, 4, True, True, True, True, False,
                                   0.1, True),
+    # Few slots and a long row: the combine's chunk is 16 KB (top-1 with a
+    # per-token bias), so each of 224 consumer threads reduces pairs of 16-byte
+    # vectors three times over and the last pass is ragged (1024 vectors).
+    "k1_wide_row_many_vectors": (300, 1, 8, 4, 16384, 75, 1, False, False, True, False, False,
+                                 0.05, False),
+    "k2_wide_row_expand": (200, 2, 8, 4, 16384, 50, 4, True, True, False, True, False, 0.05,
+                           False),
 }
 
 

@@ -62,6 +62,22 @@ __device__ __forceinline__ int chunk_of(const LayoutParams &p, int b, int &t0) {
 template <int kThreads, typename F>
 __device__ int cta_exclusive_scan(int n, F f, int32_t *out, int *warp_tot) {
   constexpr int kWarps = kThreads / 32;
+  if (n <= 32) {  // one warp's shuffle scan, one barrier
+    if (threadIdx.x < 32) {
+      const int lane = threadIdx.x;
+      const int v = lane < n ? f(lane) : 0;
+      int incl = v;
+#pragma unroll
+      for (int o = 1; o < 32; o <<= 1) {
+        const int u = __shfl_up_sync(0xffffffffu, incl, o);
+        if (lane >= o) incl += u;
+      }
+      if (lane < n) out[lane] = incl - v;
+      if (lane == 31) out[n] = incl;
+    }
+    __syncthreads();
+    return out[n];
+  }
   const int per = (n + kThreads - 1) / kThreads;
   const int beg = min((int)threadIdx.x * per, n);
   const int end = min(beg + per, n);
@@ -429,8 +445,8 @@ __global__ void __launch_bounds__(NT, 1) layout_cluster_kernel(LayoutParams p) {
   // One thread per slot: the token's lowest slot on each rank (a look-back
   // over the token's slots) sets its is_token_in_rank byte and is the rank's
   // key, counted in its ranking range (warp w < nrw ranks the slots
-  // [w * per, (w + 1) * per)); the expert counts by shared atomics.  The
-  // chunk's rank counts are the key totals, from the range bases below.
+  // [w * per, (w + 1) * per)); the expert and rank counts by shared atomics,
+  // so the chunk's counts are published right after this pass.
   const int per = max(1, (ns + nrw - 1) / nrw);
   for (int i = threadIdx.x; i < ns; i += NT) {
     const int e = idx_s[i];
@@ -450,6 +466,7 @@ __global__ void __launch_bounds__(NT, 1) layout_cluster_kernel(LayoutParams p) {
       if (own == i) {
         in_rank[t * R + r] = 1;
         key = r;
+        atomicAdd(&pub[E + r], 1);
         atomicAdd(reinterpret_cast<unsigned *>(&whist[(size_t)r * kw + i / per]), 1u);
       } else {
         key = -(own + 2);
@@ -458,8 +475,10 @@ __global__ void __launch_bounds__(NT, 1) layout_cluster_kernel(LayoutParams p) {
     loc_s[i] = key;
   }
   __syncthreads();
-  // Each range's start per rank (warp per rank, lanes = ranges); the rank's
-  // total is the chunk's count of it.
+  // This chunk's counts are published: the outputs CTA, which waits for
+  // every chunk's, starts its sums and scan while the chunks rank their slots.
+  cluster_arrive_release();
+  // Each range's start per rank (warp per rank, lanes = ranges).
   for (int r = warp; r < R; r += NWARPS) {
     unsigned long long *wk = whist + (size_t)r * kw;
     const unsigned c = lane < nrw ? (unsigned)wk[lane] : 0u;
@@ -470,10 +489,8 @@ __global__ void __launch_bounds__(NT, 1) layout_cluster_kernel(LayoutParams p) {
       if (lane >= o) incl += y;
     }
     if (lane < nrw) wk[lane] = incl - c;
-    if (lane == 31) pub[E + r] = (int)incl;
   }
   __syncthreads();
-  cluster_arrive_release();  // this chunk's counts are published
 
   // The in-order ranking overlaps the other chunks' arrival.
   if (warp < nrw)

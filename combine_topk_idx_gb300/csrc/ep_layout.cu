@@ -78,6 +78,33 @@ __device__ int cta_exclusive_scan(int n, F f, int32_t *out, int *warp_tot) {
     __syncthreads();
     return out[n];
   }
+  if (n <= kThreads) {  // one value per thread: each warp adds up its own offset
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    const int v = (int)threadIdx.x < n ? f((int)threadIdx.x) : 0;
+    int incl = v;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const int u = __shfl_up_sync(0xffffffffu, incl, o);
+      if (lane >= o) incl += u;
+    }
+    if (lane == 31) warp_tot[warp] = incl;
+    __syncthreads();
+    int before = 0, total = 0;
+    for (int w = lane; w < kWarps; w += 32) {
+      const int t = warp_tot[w];
+      total += t;
+      before += w < warp ? t : 0;
+    }
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) {
+      before += __shfl_xor_sync(0xffffffffu, before, o);
+      total += __shfl_xor_sync(0xffffffffu, total, o);
+    }
+    if ((int)threadIdx.x < n) out[threadIdx.x] = before + incl - v;
+    if (threadIdx.x == 0) out[n] = total;
+    __syncthreads();
+    return total;
+  }
   const int per = (n + kThreads - 1) / kThreads;
   const int beg = min((int)threadIdx.x * per, n);
   const int end = min(beg + per, n);
@@ -260,23 +287,14 @@ __device__ __forceinline__ void write_psum_rs(const LayoutParams &p, int b, cons
 template <int kThreads>
 __device__ __forceinline__ void write_outputs(const LayoutParams &p, const int *tot_s,
                                               const int32_t *scan_s, unsigned err) {
+  static_assert(kThreads >= 96, "three warp roles");
   const int E = p.E, R = p.R, fcap = p.fixed_cap;
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
   const int a0 = scan_s[E], r0 = scan_s[2 * E];
-  for (int e = threadIdx.x; e <= E; e += kThreads) {
-    const int pc = scan_s[e], pa = scan_s[E + e] - a0;
-    if (e < E) {
-      p.cnt_e[e] = tot_s[e];
-      p.cnt_e_al[e] = scan_s[E + e + 1] - scan_s[E + e];  // aligned count
-    }
-    p.psum_e[e] = fcap > 0 ? pc : pa;  // fixed capacity: the prefix of the counts
-    p.psum_pad[e] = pa - pc;
-  }
-  for (int r = threadIdx.x; r <= R; r += kThreads) {
-    if (r < R) p.cnt_r[r] = tot_s[E + r];
-    p.psum_r[r] = scan_s[2 * E + r] - r0;
-  }
-  if (p.disp_sync != nullptr && threadIdx.x < kDispSyncWords) p.disp_sync[threadIdx.x] = 0;
+  // Three warp roles side by side (the code of each runs once, so its
+  // instruction fetches overlap those of the others): warp 0 the control
+  // words (and the host's), warp 1 the rank outputs and the dispatch
+  // counters, the other warps the expert outputs.
   if (warp == 0) {
     err = __reduce_or_sync(0xffffffffu, err);
     bool over = false;
@@ -297,6 +315,22 @@ __device__ __forceinline__ void write_outputs(const LayoutParams &p, const int *
         p.host->num_expanded = tag | (uint32_t)num_expanded;
         p.host->error = tag | err;
       }
+    }
+  } else if (warp == 1) {
+    for (int r = lane; r <= R; r += 32) {
+      if (r < R) p.cnt_r[r] = tot_s[E + r];
+      p.psum_r[r] = scan_s[2 * E + r] - r0;
+    }
+    if (p.disp_sync != nullptr && lane < kDispSyncWords) p.disp_sync[lane] = 0;
+  } else {
+    for (int e = threadIdx.x - 64; e <= E; e += kThreads - 64) {
+      const int pc = scan_s[e], pa = scan_s[E + e] - a0;
+      if (e < E) {
+        p.cnt_e[e] = tot_s[e];
+        p.cnt_e_al[e] = scan_s[E + e + 1] - scan_s[E + e];  // aligned count
+      }
+      p.psum_e[e] = fcap > 0 ? pc : pa;  // fixed capacity: the prefix of the counts
+      p.psum_pad[e] = pa - pc;
     }
   }
 }

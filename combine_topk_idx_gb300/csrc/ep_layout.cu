@@ -13,13 +13,15 @@
 // (token, slot) inside every segment, and no atomic decides a position.  The
 // last term depends on the chunk alone.  Two forms compute the same result:
 //
-// cluster form (at most kLayoutClusterChunks chunks): one kernel, one CTA of
-//   1024 threads per chunk, the whole grid one thread-block cluster.  Each
-//   CTA loads and validates its chunk, counts experts and ranks (one thread
-//   per slot), ranks its slots, and leaves its counts in shared memory; after
-//   a cluster barrier every CTA reads the other chunks' counts through
-//   distributed shared memory, scans them into segment starts and writes its
-//   rows.  CTA 0 also writes the global counts and prefix sums.
+// cluster form (rank layouts of at most kLayoutClusterChunks chunks): one
+//   kernel, one CTA of 1024 threads per chunk plus one that owns no chunk,
+//   the whole grid one thread-block cluster.  Each chunk CTA loads and
+//   validates its chunk, counts experts and ranks (one thread per slot) in
+//   shared memory, publishes the counts (cluster barrier arrival) and ranks
+//   its slots; after the barrier it reads the other chunks' rank counts
+//   through distributed shared memory, scans them into segment starts and
+//   writes its rows.  The extra CTA sums every count over the chunks and
+//   writes the global counts and prefix sums.
 // two-kernel form (any size):
 //   count  - one thread per token: validates and copies topk_idx, builds the
 //            token's rank set (is_token_in_rank, first slot per rank) and

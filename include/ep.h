@@ -148,8 +148,10 @@ typedef struct ep_layout_info {
                                          are recv_sf[e * sf_expert_stride + i *
                                          sf_token_stride + j * sf_hidden_stride]; else 0 */
   int32_t layout_kernels;             /* kernels this layout launched: 1 (rank layouts of at
-                                         most 16 chunks of 256 tokens: one thread-block
-                                         cluster) or 2 (count + assign) */
+                                         most 15 chunks of up to 256 tokens whose counts fit
+                                         96 KB of shared memory, if the device can place the
+                                         cluster: one thread-block cluster of a CTA per chunk
+                                         plus one) or 2 (count + assign) */
   int32_t reserved1;
 } ep_layout_info;
 

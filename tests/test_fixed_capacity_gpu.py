@@ -58,7 +58,8 @@ CASES = {
     "all_slots_empty": (40, 3, 8, 4, 128, 10, False, True, True, 1.0, False),
     "empty_tokens": (0, 4, 8, 2, 128, 4, False, True, True, 0.0, False),
     "one_rank": (200, 2, 6, 1, 128, 200, True, False, False, 0.0, False),
-    # more than 16 chunks: the two-kernel layout form
+    # many layout chunks (32 and 20 source ranks; expanded layouts always take
+    # the count + assign kernels)
     "many_chunks_fp8_cm": (1000, 6, 64, 32, 256, 32, False, True, True, 0.05, False),
     "many_chunks_overflow": (40, 4, 20, 20, 128, 2, True, True, False, 0.0, True),
 }
